@@ -1,0 +1,429 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: the workload's
+copy-on-write block copies (if any), reshape_and_cache of every sequence's
+new token, then paged decode attention over context_lens tokens.  The metric
+is KV-read HBM GB/s: the K/V bytes the decode must read (sum over sequences of
+ctx * kv_heads * head_dim * element bytes * 2) divided by the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Default workload: the OPT-13B-shaped layer decode (64 sequences, 40 heads,
+head_dim 128, fp16, block size 16, context lengths U[512, 2048]).
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the path has no exchange step); the value is the bytes of all ranks divided
+by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak); µs per decode step"
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["common.cuh", "decode.cuh", "decode_launch.cuh", "decode_f32.cu",
+                  "decode_f16.cu", "decode_bf16.cu", "api.cu"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of x over ranks (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(bytes_per_rank: float, seconds_per_rank: float, world: int, device=None):
+    """Whole-job throughput: total bytes of all ranks over the slowest rank's time."""
+    total = reduce_sum(bytes_per_rank, world, device)
+    slowest = reduce_max(seconds_per_rank, world, device)
+    return total, slowest, total / slowest / 1e9
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples while the benchmark runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons), "window": "warm-up + timed steps"}
+
+
+# ------------------------------------------------------------------ peaks --
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("hbm_gbs"):
+            return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json, copy)"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def copy_peak_gbs(torch, device, stream) -> float:
+    """Same-run device copy bandwidth (read + write bytes), best of 5."""
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.uint8, device=device)
+    b = torch.empty_like(a)
+    best = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(6):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            b.copy_(a)
+            e1.record(stream)
+            e1.synchronize()
+            best = max(best, 2 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del a, b
+    return best
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_87_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: int):
+    """DRAM bytes per decode launch from a committed ncu summary, if it matches this code."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(str(workload))
+    if not rec or rec.get("source_hash") != decode_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ CPU baseline --
+
+def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int = 0):
+    """Time the fp64 oracle on whole (sequence, kv head) units of the workload.
+
+    Returns (GB/s of KV read, seconds, bytes, threads, description).  The
+    sample's pool is built by the oracle's own reshape_and_cache / copy_blocks.
+    """
+    import oracle
+    from tests.helpers import oracle_caches, oracle_decode
+    nthreads = nthreads or os.cpu_count() or 1
+    G = w.num_q_heads // w.num_kv_heads
+    e = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[w.kv_dtype]
+    kc, vc = oracle_caches(w)
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.num_seqs)
+    # calibrate on one sequence's kv head 0 group
+    s0 = int(order[0])
+    sel0 = np.array([[s0, h] for h in range(G)], np.int32)
+    t = time.perf_counter()
+    oracle_decode(w, kc, vc, sel=sel0, nthreads=1)
+    per_token_s = (time.perf_counter() - t) / max(1, int(w.context_lens[s0]))
+    budget_tokens = target_s * nthreads / max(per_token_s, 1e-9)
+    units, tokens = [], 0
+    for s in order:
+        for g in range(w.num_kv_heads):
+            units.append((int(s), g))
+            tokens += int(w.context_lens[s])
+            if tokens >= budget_tokens:
+                break
+        if tokens >= budget_tokens:
+            break
+    sel = np.array([[s, g * G + i] for s, g in units for i in range(G)], np.int32)
+    t = time.perf_counter()
+    oracle_decode(w, kc, vc, sel=sel, nthreads=nthreads)
+    secs = time.perf_counter() - t
+    nbytes = sum(int(w.context_lens[s]) for s, _ in units) * w.head_dim * e * 2
+    desc = (f"{len(units)} (sequence, kv head) units of the workload, {tokens} context tokens, "
+            f"{len(sel)} query heads, fp64 oracle on {nthreads} threads")
+    return nbytes / secs / 1e9, secs, nbytes, nthreads, desc
+
+
+# ------------------------------------------------------------------- arms --
+
+def run_ours(args, rank, world, local):
+    import torch
+    from paged_kv_cache_87_gb300 import binding, build, inputs
+    from paged_kv_cache_87_gb300.session import DeviceState, host_tensor
+
+    build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    w = inputs.make_config(args.workload)
+    st = DeviceState(w, device)
+    st.run_setup()
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize(device)
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = w.kv_read_bytes < 4 * l2
+    flush_buf = torch.empty(2 * l2 // 4 * 4 if flush else 4, dtype=torch.uint8, device=device)
+    launches_per_step = (1 if len(w.step_pairs) else 0) + 1 + 2   # copy, append, plan+decode
+
+    def step_with_decode_events(dec0, dec1):
+        st.copy_step(stream)
+        st.append_step(stream)
+        dec0.record(stream)
+        st.decode(stream)
+        dec1.record(stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st.step(stream)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(device)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            if flush:
+                flush_buf.zero_()
+            s0, d0, d1, s1 = ev[i]
+            s0.record(stream)
+            step_with_decode_events(d0, d1)
+            s1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(world)
+    clk = clocks.stop()
+    assert binding.pkv_get_device_status() == 0, "device status flagged during the benchmark"
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    sec_step = float(np.mean(step_ms)) * 1e-3
+    total_bytes, slowest, value = aggregate(w.kv_read_bytes, sec_step, world, device)
+
+    # end to end: pinned host inputs -> device, the step, result -> host, every step
+    pin = lambda t: t.pin_memory()
+    h_q = pin(host_tensor(w.query, w.q_dtype))
+    h_k = pin(host_tensor(w.key[w.new_vec], w.src_dtype))
+    h_v = pin(host_tensor(w.value[w.new_vec], w.src_dtype))
+    h_slots = pin(torch.from_numpy(w.new_slots))
+    h_ctx = pin(torch.from_numpy(w.context_lens))
+    h_tab = pin(torch.from_numpy(w.block_tables))
+    h_pairs = pin(torch.from_numpy(np.ascontiguousarray(w.step_pairs, np.int32)))
+    h_out = pin(torch.empty_like(st.out, device="cpu"))
+    ins = [(h_q, st.query), (h_k, st.new_key), (h_v, st.new_value), (h_slots, st.new_slots),
+           (h_ctx, st.context_lens), (h_tab, st.block_tables), (h_pairs, st.step_pairs)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            if flush:
+                flush_buf.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for h, d in ins:
+                d.copy_(h, non_blocking=True)
+            st.step(stream)
+            h_out.copy_(st.out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    _, _, e2e_value = aggregate(w.kv_read_bytes, float(np.mean(e2e_ms)) * 1e-3, world, device)
+
+    peak, peak_src = measured_peak()
+    dec_s = float(np.mean(dec_ms)) * 1e-3
+    achieved = w.kv_read_bytes / dec_s / 1e9
+    copy_peak = copy_peak_gbs(torch, device, stream) if rank == 0 else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(slowest * 1e3, 5),
+        "us_per_step": round(slowest * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.q_dtype if w.kv_dtype != "e4m3" else "bf16+e4m3",
+        "data": "synthetic (seeded N(0,1) q/K/V; seeded block permutation)",
+        "config": {
+            "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "kv_dtype": w.kv_dtype,
+            "mean_context": float(w.context_lens.mean()),
+            "kv_read_bytes_per_step": w.kv_read_bytes,
+            "l2": ("L2 flushed between steps (write of 2x L2)" if flush else
+                   f"inputs larger than L2 ({w.kv_read_bytes / 1e9:.2f} GB of KV per step)"),
+            "step": "copy_blocks (if any) + reshape_and_cache + paged decode",
+            "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(args.workload),
+                     "kernel": "plan + decode_simt (events around the decode call)",
+                     "decode_us": round(dec_s * 1e6, 2)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "copy_peak_gbs_same_run": round(copy_peak, 1) if copy_peak else None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, nbytes, threads, desc = oracle_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc,
+                                "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world, local):
+    """The oracle, as it stands, on host cores: each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from paged_kv_cache_87_gb300 import inputs
+    import oracle
+    oracle.build()
+    w = inputs.make_config(args.workload)
+    per_step = max(0.2, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
+    vals, secs, desc, threads = [], [], "", 1
+    for i in range(args.warmup + args.steps):
+        v, s, _, threads, desc = oracle_baseline(w, per_step, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+            secs.append(s)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(float(np.mean(secs)) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "kv_dtype": w.kv_dtype},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": "per step: " + desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world, local)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

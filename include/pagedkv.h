@@ -1,0 +1,203 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the data-parallel hot path of
+ * PagedAttention on one GB300 (sm_103a).
+ *
+ * Three operations, after "PagedAttention: Mathematical Foundations, Virtual
+ * Memory Block Allocation, and Zero-Waste KV Cache Serving" (llms.blog):
+ *   - pkv_paged_decode_attention: §3 (block-wise attention over a context
+ *     split into B-token blocks) and §7 kernel 2 / the decode pseudocode
+ *     (one pass over the block table with a running max, rescale and sum);
+ *   - pkv_reshape_and_cache: §7 kernel 1 (write each new token's key and
+ *     value straight into its physical block slot);
+ *   - pkv_copy_blocks: §5 Parallel Sampling step 4 and §7 kernel 3 (all
+ *     copy-on-write block copies of a step in one launch).
+ *
+ * Conventions shared by every call
+ *   Memory:  every pointer argument except `host_code` is a DEVICE pointer
+ *            on the current CUDA device.  The caller owns every buffer,
+ *            including the decode workspace; the library never allocates.
+ *   Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *            All calls are stream-ordered and asynchronous; none synchronises
+ *            the device (pkv_get_device_status excepted).
+ *   Errors:  scalar/pointer/alignment checks run on the host before any
+ *            launch and return a pkv_status without touching the GPU.  A
+ *            failed launch returns PKV_ERR_CUDA.  Contract violations that
+ *            live in device data (a block id outside the pool, a context
+ *            length above the table's capacity, a slot outside the pool) are
+ *            caught by the kernels, which skip the offending access (never
+ *            trapping) and set a bit in a per-device status word that
+ *            pkv_get_device_status reads.
+ *
+ * KV cache layout (this library's contract; the pages disagree with each
+ * other -- "Pytorch implementation of paper ..." (aishastr.live) §2 stores K
+ * as [blocks, heads, head_dim, B], the 10100.com page §2 quotes a 5-D K and a
+ * head_dim-major V): k_cache and v_cache are both
+ *     [num_blocks][num_kv_heads][block_size][head_dim], head_dim contiguous,
+ * so every (physical block, kv head) tile is one contiguous run of
+ * block_size * head_dim elements.  Token row `off` of physical block `blk`
+ * holds logical position j*B + off of every sequence whose table entry j is
+ * `blk`.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  PKV_FP8_E4M3 is the OCP 8-bit "e4m3fn" format (bias 7, no
+ * infinities, S.1111.111 = NaN, largest finite 448); it is a KV storage type
+ * only. */
+typedef enum pkv_dtype {
+    PKV_F32 = 0,
+    PKV_F16 = 1,
+    PKV_BF16 = 2,
+    PKV_FP8_E4M3 = 3
+} pkv_dtype;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad scale */
+    PKV_ERR_UNSUPPORTED = 2,   /* head_dim, block_size or dtype combination not built */
+    PKV_ERR_WORKSPACE = 3,     /* decode workspace too small or misaligned */
+    PKV_ERR_CUDA = 4           /* a CUDA runtime call or launch failed */
+} pkv_status;
+
+/* Bits of the device status word (see pkv_get_device_status). */
+#define PKV_DEV_BAD_BLOCK_ID   0x1u  /* table entry outside [0, num_blocks): block skipped */
+#define PKV_DEV_BAD_CONTEXT    0x2u  /* context_len < 0 or above max_context_len or
+                                        max_blocks_per_seq * block_size: clamped */
+#define PKV_DEV_BAD_SLOT       0x4u  /* slot >= num_blocks * block_size: token skipped */
+#define PKV_DEV_BAD_PAIR       0x8u  /* copy pair id outside [0, num_blocks): pair skipped */
+#define PKV_DEV_WAIT_TIMEOUT   0x10u /* a pipeline wait exceeded its bound: kernel returned */
+
+/* Symbols of the C ABI are the only ones the library exports. */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+/* Opaque stand-in for cudaStream_t, so this header needs no CUDA include. */
+typedef struct CUstream_st* pkv_stream_t;
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attention needs for these sizes.
+ * The workspace holds the per-call work list, one arrival counter per
+ * (sequence, kv head group) and the split-KV partial states (m, l, acc[d]) of
+ * every chunk of every (sequence, query head).  It need not be zeroed.
+ * Returns 0 for unsupported or invalid sizes.
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int max_context_len,
+                                  pkv_dtype kv_dtype);
+
+/*
+ * Single-query decode attention over a paged KV cache.
+ *
+ * For every sequence s and query head h (kv head g = h / (num_q_heads /
+ * num_kv_heads), contiguous GQA groups), over the context_lens[s] tokens
+ * whose rows are found through block_tables[s][t / block_size], row
+ * t % block_size:
+ *     out[s][h] = sum_t softmax_t(scale * q[s][h] . k_t) * v_t
+ * ("...Mathematical Foundations" §3: a_ij and o_i; the kernel evaluates it
+ * in one pass with the running-max rescale of §7's pseudocode, splitting long
+ * contexts into chunks whose partial states are merged by the same rescale).
+ * A sequence with context_len 0 gets an all-zero output.
+ * With kv_dtype PKV_FP8_E4M3 every K/V element is decode(code) * kv_scale.
+ *
+ *   query         [num_seqs][num_q_heads][head_dim], q_dtype, 16-byte aligned
+ *   k_cache,
+ *   v_cache       [num_blocks][num_kv_heads][block_size][head_dim], kv_dtype,
+ *                 16-byte aligned (layout above); rows at or beyond a
+ *                 sequence's context length are never used (may hold NaN)
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                 ceil(context_lens[s] / block_size) entries of a row are read
+ *   context_lens  int32 [num_seqs]
+ *   max_context_len  host-known upper bound of context_lens (sizes the
+ *                 workspace and the split plan); must be <= max_blocks_per_seq
+ *                 * block_size.  Longer device values are clamped to it and
+ *                 flagged PKV_DEV_BAD_CONTEXT.
+ *   scale         logit scale (1/sqrt(head_dim) for standard attention)
+ *   q_dtype       PKV_F32 / PKV_F16 / PKV_BF16; out has the same type
+ *   kv_dtype      q_dtype or PKV_FP8_E4M3
+ *   kv_scale      dequantisation scale for FP8 KV (> 0, finite; pass 1 otherwise)
+ *   workspace     device buffer of >= pkv_decode_workspace_bytes(...) bytes,
+ *                 256-byte aligned; calls sharing a workspace must be ordered
+ *                 on one stream
+ *   out           [num_seqs][num_q_heads][head_dim], q_dtype, 16-byte aligned
+ * Supported: head_dim in {64, 128}; block_size in {8, 16, 32}; any
+ * num_q_heads that is a multiple of num_kv_heads.
+ * Two launches on `stream`: a one-CTA planning kernel and the decode kernel.
+ */
+PKV_API pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks,
+                                      int max_blocks_per_seq, int max_context_len, float scale,
+                                      pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale,
+                                      void* workspace, size_t workspace_bytes, void* out,
+                                      pkv_stream_t stream);
+
+/*
+ * Write new tokens' keys and values into their cache slots
+ * ("...Mathematical Foundations" §7 kernel 1; §4 Allocation Lifecycle step 2).
+ *
+ * For every token t with slot_mapping[t] >= 0 and every kv head h:
+ *   block = slot / block_size, row = slot % block_size,
+ *   k_cache[block][h][row][:] = key[t][h][:]   (same for value / v_cache).
+ * Same element type: a bit copy.  kv_dtype PKV_FP8_E4M3: each element becomes
+ * e4m3(x / kv_scale), the quotient taken in fp32 with IEEE rounding, then
+ * rounded to nearest-even with saturation to +-448 (NaN stays NaN).
+ *
+ *   key, value    [num_tokens][num_kv_heads][head_dim], src_dtype, contiguous,
+ *                 16-byte aligned
+ *   slot_mapping  int64 [num_tokens]; negative = padding, skipped; slots at or
+ *                 beyond num_blocks * block_size are skipped and flagged
+ *                 PKV_DEV_BAD_SLOT.  Two tokens with the same slot race.
+ *   src_dtype     PKV_F32 / PKV_F16 / PKV_BF16;  kv_dtype: src_dtype or FP8
+ * One launch on `stream` (none when num_tokens == 0).
+ */
+PKV_API pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                                 void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 pkv_dtype src_dtype, pkv_dtype kv_dtype, float kv_scale,
+                                 pkv_stream_t stream);
+
+/*
+ * Batched copy-on-write ("...Mathematical Foundations" §5 step 4, §7 kernel 3):
+ * for every pair i, physical block pairs[i][1] of both caches becomes a byte
+ * copy of block pairs[i][0] (all kv heads), in one launch.
+ *
+ *   src_dst_pairs int32 [num_pairs][2] (device).  The dst ids must be distinct
+ *                 and no dst may also be a src (the result would depend on
+ *                 order); the library cannot check this without reading the
+ *                 pairs back, so callers validate it.  Ids outside the pool
+ *                 are skipped and flagged PKV_DEV_BAD_PAIR.
+ * One launch on `stream` (none when num_pairs == 0).
+ */
+PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs,
+                           int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, pkv_dtype kv_dtype, pkv_stream_t stream);
+
+/*
+ * Read and clear the status word of the current device (a bit-or of
+ * PKV_DEV_* flags set by kernels since the last read).  Synchronous: waits
+ * for the device's work to finish.  `host_code` is a host pointer.
+ */
+PKV_API pkv_status pkv_get_device_status(unsigned int* host_code);
+
+/* Static description of a pkv_status. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+PKV_API int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

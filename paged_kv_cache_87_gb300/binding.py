@@ -1,0 +1,228 @@
+"""ctypes binding of libpagedkv.so (C ABI: include/pagedkv.h).
+
+Argument marshalling only: shapes, dtypes and the stream are read off torch
+tensors and passed as plain pointers and sizes; every step of the hot path
+runs in the library's CUDA kernels.  There is no CPU fallback: if the library
+cannot be loaded the calls raise.
+
+Functions carry the C names:
+  pkv_decode_workspace_bytes, pkv_paged_decode_attention,
+  pkv_reshape_and_cache, pkv_copy_blocks, pkv_get_device_status,
+  pkv_status_string, pkv_version.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2, 3
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT = (
+    0x1, 0x2, 0x4, 0x8, 0x10)
+
+# ctypes signatures of every exported symbol
+_SIGNATURES = {
+    "pkv_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6 + [ctypes.c_int]),
+    "pkv_paged_decode_attention": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_float, ctypes.c_void_p,
+                                                     ctypes.c_size_t, ctypes.c_void_p,
+                                                     ctypes.c_void_p]),
+    "pkv_reshape_and_cache": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                                     ctypes.c_void_p]),
+    "pkv_copy_blocks": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_int, ctypes.c_void_p]),
+    "pkv_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_version": (ctypes.c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_text(status)} (status {status})")
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (build it first with ``paged_kv_cache_87_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m paged_kv_cache_87_gb300.build` (needs nvcc)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype, f.argtypes = res, args
+            _lib = lib
+        return _lib
+
+
+def status_text(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != PKV_OK:
+        raise PagedKVError(fn, status)
+
+
+_TORCH_CODES = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16,
+                torch.float8_e4m3fn: PKV_FP8_E4M3, torch.uint8: PKV_FP8_E4M3}
+_NAME_CODES = {"f32": PKV_F32, "f16": PKV_F16, "bf16": PKV_BF16, "e4m3": PKV_FP8_E4M3}
+
+
+def dtype_code(x) -> int:
+    if isinstance(x, torch.Tensor):
+        return _TORCH_CODES[x.dtype]
+    if isinstance(x, torch.dtype):
+        return _TORCH_CODES[x]
+    if isinstance(x, str):
+        return _NAME_CODES[x]
+    return int(x)
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+# ------------------------------------------------------------------ calls --
+
+def pkv_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                               block_size: int, max_context_len: int, kv_dtype) -> int:
+    return int(load().pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_context_len,
+                                                 dtype_code(kv_dtype)))
+
+
+def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               max_context_len: int, scale: float, kv_scale: float = 1.0,
+                               workspace: torch.Tensor | None = None,
+                               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s over context_lens[s] tokens.
+
+    query [S, Hq, d]; k_cache / v_cache [NB, Hkv, B, d] (float8_e4m3fn or uint8
+    for FP8); block_tables int32 [S, max_blocks]; context_lens int32 [S].
+    ``workspace`` (uint8, >= pkv_decode_workspace_bytes) is allocated if None.
+    """
+    S, Hq, d = query.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    for t, n in ((query, "query"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens")):
+        _cuda(t, n)
+    qc, kc = dtype_code(query), dtype_code(k_cache)
+    need = pkv_decode_workspace_bytes(S, Hq, Hkv, d, B, max_context_len, kc)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _cuda(workspace, "workspace")
+    st = load().pkv_paged_decode_attention(
+        query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), S, Hq, Hkv, d, B, NB, block_tables.shape[1],
+        int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
+    _check("pkv_paged_decode_attention", st)
+    return out
+
+
+def pkv_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          kv_scale: float = 1.0, stream=None) -> None:
+    """k_cache[slot // B, h, slot % B] = key[t, h] (e4m3(x / kv_scale) for FP8 caches)."""
+    T, Hkv, d = key.shape
+    NB, Hkv2, B, d2 = k_cache.shape
+    if (Hkv2, d2) != (Hkv, d) or tuple(value.shape) != tuple(key.shape):
+        raise ValueError("key/value [T, Hkv, d] do not match the cache [NB, Hkv, B, d]")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    for t, n in ((key, "key"), (value, "value"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (slot_mapping, "slot_mapping")):
+        _cuda(t, n)
+    st = load().pkv_reshape_and_cache(
+        key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        slot_mapping.data_ptr(), T, Hkv, d, B, NB, dtype_code(key), dtype_code(k_cache),
+        float(kv_scale), _stream_ptr(stream))
+    _check("pkv_reshape_and_cache", st)
+
+
+def validate_pairs(pairs: np.ndarray, num_blocks: int) -> None:
+    """Host check of the copy_blocks contract: ids in the pool, distinct dsts, no dst is a src."""
+    pairs = np.asarray(pairs).reshape(-1, 2)
+    if pairs.size and (pairs.min() < 0 or pairs.max() >= num_blocks):
+        raise ValueError("copy_blocks: block id outside the pool")
+    dst = pairs[:, 1]
+    if len(set(dst.tolist())) != len(dst):
+        raise ValueError("copy_blocks: a destination block repeats")
+    if set(dst.tolist()) & set(pairs[:, 0].tolist()):
+        raise ValueError("copy_blocks: a destination block is also a source")
+
+
+def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
+                    stream=None) -> None:
+    """Copy physical blocks src -> dst of both caches for every (src, dst) pair.
+
+    ``src_dst_pairs``: int32 [n, 2].  A host array/tensor is validated and
+    copied to the device; a CUDA tensor is used as is (the caller has
+    validated it).
+    """
+    NB, Hkv, B, d = k_cache.shape
+    _cuda(k_cache, "k_cache")
+    _cuda(v_cache, "v_cache")
+    if isinstance(src_dst_pairs, torch.Tensor) and src_dst_pairs.is_cuda:
+        pairs = src_dst_pairs
+    else:
+        host = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int32).reshape(-1, 2))
+        validate_pairs(host, NB)
+        pairs = torch.from_numpy(host).to(k_cache.device)
+    if pairs.dtype != torch.int32:
+        raise ValueError("src_dst_pairs must be int32")
+    n = pairs.numel() // 2
+    st = load().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
+                                pairs.data_ptr() if n else None, n, Hkv, d, B, NB,
+                                dtype_code(k_cache), _stream_ptr(stream))
+    _check("pkv_copy_blocks", st)
+
+
+def pkv_get_device_status() -> int:
+    """Read and clear the current device's status word (PKV_DEV_* bits). Synchronous."""
+    v = ctypes.c_uint(0)
+    _check("pkv_get_device_status", load().pkv_get_device_status(ctypes.byref(v)))
+    return int(v.value)
+
+
+def pkv_status_string(status: int) -> str:
+    return status_text(status)
+
+
+def pkv_version() -> int:
+    return int(load().pkv_version())

@@ -1,0 +1,60 @@
+// decode_launch.cuh -- host-side launch of the planning + decode kernels for
+// one query type.  Each decode_<qtype>.cu includes this and instantiates the
+// (kv type, head_dim, heads-per-item) variants it serves, so the variants
+// compile in parallel translation units.
+#pragma once
+
+#include "decode.cuh"
+
+namespace pkv {
+
+// Per-device cache of a kernel's resident CTAs per SM (0 = not yet queried).
+struct OccCache {
+    int ctas[64] = {0};
+};
+
+template <typename QT, typename KT, int HD, int HPI>
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
+    using Cfg = SimtCfg<QT, KT, HD, HPI>;
+    const size_t smem = SimtSmem<Cfg>::total;
+    static OccCache occ;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kernel = decode_simt_kernel<QT, KT, HD, HPI>;
+    if (occ.ctas[dev] == 0) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        int per_sm = 0, sms = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Cfg::THREADS, smem);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        occ.ctas[dev] = (per_sm > 0 ? per_sm : 1) * sms;
+    }
+    plan_kernel<QT><<<1, 1024, 0, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    kernel<<<occ.ctas[dev], Cfg::THREADS, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename QT, typename KT>
+cudaError_t dispatch_decode_kv(const DecodeParams& p, int hpi, cudaStream_t stream) {
+    if (p.head_dim == 128) {
+        if (hpi == 1) return launch_decode_simt<QT, KT, 128, 1>(p, stream);
+        if (hpi == 2) return launch_decode_simt<QT, KT, 128, 2>(p, stream);
+        return launch_decode_simt<QT, KT, 128, 4>(p, stream);
+    }
+    if (hpi == 1) return launch_decode_simt<QT, KT, 64, 1>(p, stream);
+    if (hpi == 2) return launch_decode_simt<QT, KT, 64, 2>(p, stream);
+    return launch_decode_simt<QT, KT, 64, 4>(p, stream);
+}
+
+// Defined in decode_f32.cu / decode_f16.cu / decode_bf16.cu.
+cudaError_t decode_dispatch_f32(const DecodeParams& p, pkv_dtype kv, int hpi, cudaStream_t s);
+cudaError_t decode_dispatch_f16(const DecodeParams& p, pkv_dtype kv, int hpi, cudaStream_t s);
+cudaError_t decode_dispatch_bf16(const DecodeParams& p, pkv_dtype kv, int hpi, cudaStream_t s);
+
+}  // namespace pkv

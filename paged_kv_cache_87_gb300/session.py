@@ -1,0 +1,110 @@
+"""Device-side state of a workload: the pool, tables and step inputs in HBM.
+
+Allocation is torch's (device memory and streams are torch's job here); every
+write into the pool and the decode itself go through the C ABI (``binding``).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding
+from .inputs import Workload
+
+TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+               "e4m3": torch.float8_e4m3fn}
+
+
+def host_tensor(a: np.ndarray, dtype: str) -> torch.Tensor:
+    """Wrap a numpy storage array (bf16 as uint16, e4m3 as uint8) as a torch tensor."""
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    if dtype == "e4m3":
+        return torch.from_numpy(a.view(np.uint8)).view(torch.float8_e4m3fn)
+    return torch.from_numpy(a)
+
+
+def poisoned_cache(shape, dtype: str, device) -> torch.Tensor:
+    t = torch.empty(shape, dtype=TORCH_DTYPE[dtype], device=device)
+    if dtype == "e4m3":
+        t.view(torch.uint8).fill_(0x7F)        # E4M3 NaN
+    else:
+        t.fill_(float("nan"))
+    return t
+
+
+def to_numpy_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if dtype == "bf16":
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if dtype == "e4m3":
+        return t.view(torch.uint8).numpy()
+    return t.numpy()
+
+
+class DeviceState:
+    """A workload's pool and step inputs resident on one CUDA device."""
+
+    def __init__(self, w: Workload, device="cuda", keep_vectors: bool = False):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.k_cache = poisoned_cache(w.cache_shape, w.kv_dtype, dev)
+        self.v_cache = poisoned_cache(w.cache_shape, w.kv_dtype, dev)
+        self.query = host_tensor(w.query, w.q_dtype).to(dev)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.context_lens = torch.from_numpy(w.context_lens).to(dev)
+        self.step_pairs = torch.from_numpy(np.ascontiguousarray(w.step_pairs, np.int32)).to(dev)
+        self.new_key = host_tensor(w.key[w.new_vec], w.src_dtype).to(dev)
+        self.new_value = host_tensor(w.value[w.new_vec], w.src_dtype).to(dev)
+        self.new_slots = torch.from_numpy(w.new_slots).to(dev)
+        self.out = torch.empty_like(self.query)
+        self.workspace = torch.empty(
+            max(256, binding.pkv_decode_workspace_bytes(
+                w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                w.max_context_len, w.kv_dtype)), dtype=torch.uint8, device=dev)
+        self.keep_vectors = keep_vectors
+
+    # ---------------------------------------------------------------- setup --
+    def run_setup(self, chunk_tokens: int = 1 << 20) -> None:
+        """Fill the pool: the workload's prefill writes and fork copies, in order."""
+        w = self.w
+        for op in w.setup:
+            if op[0] == "copy":
+                binding.pkv_copy_blocks(self.k_cache, self.v_cache, op[1])
+                continue
+            idx, slots = op[1], op[2]
+            for a in range(0, len(idx), chunk_tokens):
+                sl = slice(a, a + chunk_tokens)
+                k = host_tensor(w.key[idx[sl]], w.src_dtype).to(self.device)
+                v = host_tensor(w.value[idx[sl]], w.src_dtype).to(self.device)
+                s = torch.from_numpy(np.ascontiguousarray(slots[sl])).to(self.device)
+                binding.pkv_reshape_and_cache(k, v, self.k_cache, self.v_cache, s,
+                                              kv_scale=w.kv_scale)
+        torch.cuda.synchronize(self.device)
+
+    # ----------------------------------------------------------------- step --
+    def copy_step(self, stream=None) -> None:
+        if self.step_pairs.numel():
+            binding.pkv_copy_blocks(self.k_cache, self.v_cache, self.step_pairs, stream=stream)
+
+    def append_step(self, stream=None) -> None:
+        binding.pkv_reshape_and_cache(self.new_key, self.new_value, self.k_cache, self.v_cache,
+                                      self.new_slots, kv_scale=self.w.kv_scale, stream=stream)
+
+    def decode(self, stream=None, out=None) -> torch.Tensor:
+        w = self.w
+        return binding.pkv_paged_decode_attention(
+            self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+            w.max_context_len, w.scale, kv_scale=w.kv_scale, workspace=self.workspace,
+            out=self.out if out is None else out, stream=stream)
+
+    def step(self, stream=None) -> torch.Tensor:
+        """One pass of the hot path: copy-on-write, append the new tokens, decode."""
+        self.copy_step(stream)
+        self.append_step(stream)
+        return self.decode(stream)
+
+    def out_f64(self) -> np.ndarray:
+        return self.out.detach().to(torch.float64).cpu().numpy()

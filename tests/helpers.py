@@ -92,3 +92,47 @@ def logical_kv_f64(w: inputs.Workload, s: int):
     """
     idx = w.seq_tokens[s]
     return to_f64(w.key[idx], w.src_dtype), to_f64(w.value[idx], w.src_dtype)
+
+
+# ------------------------------------------------------------- GPU side --
+
+# max abs error allowed against the fp64 oracle, by the type that limits precision
+TOL = {"f32": 1e-4, "f16": 5e-3, "bf16": 1.6e-2, "e4m3": 1.6e-2}
+
+
+def tolerance(w: inputs.Workload) -> float:
+    return TOL["e4m3"] if w.kv_dtype == "e4m3" else TOL[w.q_dtype]
+
+
+def gpu_state(w: inputs.Workload, steps: int = 1):
+    """DeviceState after the workload's setup and `steps` hot-path steps."""
+    import torch
+    from paged_kv_cache_87_gb300 import binding
+    from paged_kv_cache_87_gb300.session import DeviceState
+    st = DeviceState(w, "cuda")
+    st.run_setup()
+    for _ in range(steps):
+        st.step()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() == 0
+    return st
+
+
+def relabel_blocks(w: inputs.Workload, perm: np.ndarray) -> inputs.Workload:
+    """The same workload with physical block b renamed perm[b] everywhere."""
+    import dataclasses
+    B = w.block_size
+
+    def slots(a):
+        a = np.asarray(a, np.int64)
+        return np.where(a >= 0, perm[np.maximum(a, 0) // B] * B + np.maximum(a, 0) % B, a)
+
+    def pairs(p):
+        return perm[np.asarray(p, np.int64)].astype(np.int32).reshape(-1, 2)
+
+    setup = [(op[0], op[1], slots(op[2])) if op[0] == "reshape" else (op[0], pairs(op[1]))
+             for op in w.setup]
+    tables = np.where(w.block_tables >= 0, perm[np.maximum(w.block_tables, 0)], -1)
+    return dataclasses.replace(w, setup=setup, step_pairs=pairs(w.step_pairs),
+                               new_slots=slots(w.new_slots),
+                               block_tables=tables.astype(np.int32))

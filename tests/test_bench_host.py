@@ -1,0 +1,86 @@
+"""Host-side logic of bench.py, on CPU: replica aggregation over 2 gloo ranks,
+clock-sample parsing, and the traffic record's source check."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r processed (r+1) GB in (r+1)*0.5 s: slowest rank 1.0 s, total 3 GB
+    total, slowest, gbs = bench.aggregate((rank + 1) * 1e9, (rank + 1) * 0.5, world)
+    bench.barrier(world)
+    q.put((rank, total, slowest, gbs))
+    dist.destroy_process_group()
+
+
+def test_replica_aggregation_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, total, slowest, gbs in res:
+        assert total == pytest.approx(3e9)
+        assert slowest == pytest.approx(1.0)
+        assert gbs == pytest.approx(3.0)
+
+
+def test_single_rank_aggregation_is_identity():
+    total, slowest, gbs = bench.aggregate(2e9, 0.5, 1)
+    assert (total, slowest, gbs) == (2e9, 0.5, 4.0)
+
+
+def test_clock_sampler_parsing():
+    c = bench.ClockSampler(0)
+    c.proc = type("P", (), {"terminate": lambda s: None, "wait": lambda s, timeout: 0})()
+    c.lines = ["0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1980, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "garbage"]
+    r = c.stop()
+    assert r["sm_mhz"] == pytest.approx(1972.5)
+    assert r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_traffic_record_requires_matching_source(tmp_path, monkeypatch):
+    h = bench.decode_source_hash()
+    assert len(h) == 16
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "decode_traffic.json").write_text(json.dumps(
+        {"1": {"source_hash": h, "dram_bytes_per_launch": 123},
+         "2": {"source_hash": "stale", "dram_bytes_per_launch": 456}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "decode_source_hash", lambda: h)
+    assert bench.recorded_traffic(1) == 123
+    assert bench.recorded_traffic(2) is None
+    assert bench.recorded_traffic(3) is None
+
+
+def test_peak_falls_back_without_measured_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6785.2}))
+    assert bench.measured_peak()[0] == 6785.2

@@ -1,0 +1,208 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Small workloads are compared element by element; the five workloads at full
+size are compared on sampled (sequence, head) outputs in the same launch
+configuration the benchmark times.  Tolerances: max abs error 1e-4 (fp32),
+5e-3 (fp16), 1.6e-2 (bf16), 1.6e-2 (FP8 KV against the oracle's decode of the
+same bytes).
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_87_gb300 import binding, inputs
+from tests.helpers import (gpu_state, logical_kv_f64, oracle_caches, oracle_decode,
+                           relabel_blocks, tolerance, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, got, ref, sel=None):
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert err.max() <= tolerance(w), (err.max(), tolerance(w), np.unravel_index(err.argmax(),
+                                                                                  err.shape))
+
+
+def _full_parity(w):
+    st = gpu_state(w)
+    kc, vc = oracle_caches(w)
+    ref = oracle_decode(w, kc, vc, nthreads=8)
+    _check(w, st.out_f64(), ref)
+    return st, ref
+
+
+# ------------------------------------------------ the five workloads, small --
+
+@pytest.mark.parametrize("cid,kw", [
+    (0, {}),                                    # full size: 4 seqs, ctx {1,17,100,256}
+    (1, dict(num_seqs=6)),                      # ctx U[512,2048]: multi-chunk merge
+    (2, dict(num_seqs=24)),                     # lognormal lengths, GQA 4
+    (3, dict(num_seqs=2, ctx_cap=6000)),        # GQA 8, B32, long-ish
+    (4, dict(num_seqs=8, ctx_cap=1500)),        # FP8 + shared prefix + CoW step
+])
+def test_config_small_elementwise(cid, kw):
+    _full_parity(inputs.make_config(cid, **kw))
+
+
+# ---------------------------------------------- the workloads at full size --
+
+def _sample_pairs(w, n, seed):
+    rng = np.random.default_rng(seed)
+    longest = int(np.argmax(w.context_lens))
+    shortest = int(np.argmin(w.context_lens))
+    seqs = np.concatenate([[longest, shortest], rng.integers(0, w.num_seqs, n - 2)])
+    heads = rng.integers(0, w.num_q_heads, n)
+    heads[:2] = [0, w.num_q_heads - 1]
+    return np.stack([seqs, heads], 1).astype(np.int32)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4])
+def test_config_full_size_sampled(cid):
+    w = inputs.make_config(cid)
+    st = gpu_state(w, steps=2)          # steps are idempotent; run the bench's step twice
+    sel = _sample_pairs(w, 24, cid)
+    kc, vc = oracle_caches(w)
+    ref = oracle_decode(w, kc, vc, sel=sel, nthreads=8)
+    out = st.out_f64()
+    got = out[sel[:, 0], sel[:, 1]]
+    _check(w, got, ref)
+    # every output is finite; zero-context sequences are zero
+    assert np.isfinite(out).all()
+
+
+# --------------------------------------------------------------- sweeps ----
+
+SWEEP = []
+for d in (64, 128):
+    for B in (8, 16, 32):
+        for (Hq, Hkv) in ((4, 4), (6, 2), (8, 2), (10, 2), (16, 2)):
+            SWEEP.append((d, B, Hq, Hkv))
+
+
+@pytest.mark.parametrize("d,B,Hq,Hkv", SWEEP)
+@pytest.mark.parametrize("qdt,kvdt", [("f32", "f32"), ("f16", "f16"), ("bf16", "bf16"),
+                                      ("bf16", "e4m3")])
+def test_sweep_shapes_and_types(d, B, Hq, Hkv, qdt, kvdt):
+    if (d, B) != (128, 16) and (qdt, kvdt) not in (("f32", "f32"), ("bf16", "e4m3")):
+        pytest.skip("dtype x shape product thinned: every shape runs f32 and fp8")
+    rng = np.random.default_rng(zlib.crc32(repr((d, B, Hq, Hkv, qdt, kvdt)).encode()))
+    ctx = np.array([1, B - 1, B, B + 1, 511, 512, 513, 1100, 0, 3000])
+    w = inputs.make_independent("sweep", rng, ctx, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
+                                block_size=B, q_dtype=qdt, kv_dtype=kvdt,
+                                scale=1.0 / math.sqrt(d),
+                                kv_scale=2.0 ** -5 if kvdt == "e4m3" else 1.0)
+    st, _ = _full_parity(w)
+    assert (st.out_f64()[8] == 0).all()          # context 0 -> zeros
+
+
+# ------------------------------------------------------------ properties --
+
+def _tiny(seed, ctx, **kw):
+    rng = np.random.default_rng(seed)
+    a = dict(num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, q_dtype="f32",
+             kv_dtype="f32", scale=1 / math.sqrt(128))
+    a.update(kw)
+    if a["kv_dtype"] == "e4m3":
+        a.setdefault("kv_scale", 2.0 ** -5)
+    return inputs.make_independent("tiny", rng, np.array(ctx), **a)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_context_one_returns_v1_bit_exact(dt):
+    w = _tiny(1, [1] * 5, q_dtype=dt, kv_dtype=dt)
+    st = gpu_state(w)
+    out = st.out.cpu()
+    G = w.num_q_heads // w.num_kv_heads
+    for s in range(5):
+        v = torch.from_numpy(np.ascontiguousarray(w.value[w.seq_tokens[s][0]]))
+        if dt == "bf16":
+            v = v.view(torch.int16).view(torch.bfloat16)
+        assert torch.equal(out[s], v.repeat_interleave(G, 0))
+
+
+def test_constant_values_give_the_constant():
+    w = _tiny(2, [5, 100, 700, 2500], values="constant_v")
+    st = gpu_state(w)
+    v = to_f64(w.value[0], "f32")
+    np.testing.assert_allclose(st.out_f64(), np.repeat(v, 4, 0)[None].repeat(4, 0), atol=2e-6)
+
+
+def test_physical_block_permutation_is_bit_identical():
+    w = _tiny(3, [7, 300, 1200, 2049], q_dtype="bf16", kv_dtype="bf16")
+    a = gpu_state(w).out.clone()
+    perm = np.random.default_rng(9).permutation(w.num_blocks)
+    b = gpu_state(relabel_blocks(w, perm)).out.clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_repeated_decode_is_bit_identical():
+    w = _tiny(4, [3000, 4100, 90, 513], q_dtype="f16", kv_dtype="f16")
+    st = gpu_state(w)
+    first = st.out.clone()
+    for _ in range(3):
+        st.decode()
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), st.out.view(torch.int16))
+
+
+def test_nan_poison_outside_context_is_never_read():
+    """The pool starts as NaN everywhere; only rows below context_len are written."""
+    w = _tiny(5, [1, 15, 17, 33, 1000], q_dtype="bf16", kv_dtype="e4m3")
+    st = gpu_state(w)
+    assert torch.isfinite(st.out.float()).all()
+
+
+def test_shared_prefix_cow_step_is_bit_identical():
+    w = inputs.make_config(4, num_seqs=16, ctx_cap=2000)
+    st = gpu_state(w)
+    with_cow = st.out.clone()
+    tables = w.block_tables.copy()
+    for src, dst in w.step_pairs:
+        tables[tables == dst] = src
+    st.block_tables.copy_(torch.from_numpy(tables))
+    st.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(with_cow.view(torch.int16), st.out.view(torch.int16))
+
+
+def test_matches_dense_attention_on_logical_kv():
+    """Independent of both caches: dense fp64 attention on the generator's logical rows."""
+    w = _tiny(6, [40, 600, 1500], q_dtype="f32", kv_dtype="f32", num_q_heads=4,
+              num_kv_heads=4)
+    st = gpu_state(w)
+    q = to_f64(w.query, "f32")
+    for s in range(3):
+        K, V = logical_kv_f64(w, s)
+        for h in range(4):
+            z = w.scale * K[:, h] @ q[s, h]
+            p = np.exp(z - z.max())
+            ref = p @ V[:, h] / p.sum()
+            assert np.abs(st.out_f64()[s, h] - ref).max() <= 1e-4
+
+
+# ------------------------------------------------------- device contract --
+
+def test_bad_block_id_is_flagged_not_faulted():
+    w = _tiny(7, [40, 40])
+    st = gpu_state(w)
+    bad = st.block_tables.clone()
+    bad[1, 1] = w.num_blocks + 1000
+    st.block_tables.copy_(bad)
+    st.decode()
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_BLOCK_ID
+
+
+def test_context_above_max_context_len_is_clamped_and_flagged():
+    w = _tiny(8, [40, 100])
+    st = gpu_state(w)
+    binding.pkv_paged_decode_attention(st.query, st.k_cache, st.v_cache, st.block_tables,
+                                       st.context_lens, 64, w.scale, workspace=st.workspace,
+                                       out=st.out)
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_CONTEXT
+    kc, vc = oracle_caches(w)
+    ref = oracle_decode(w, kc, vc, context_lens=np.minimum(w.context_lens, 64))
+    _check(w, st.out_f64(), ref)
