@@ -184,6 +184,37 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* 
                            int num_blocks, pkv_dtype kv_dtype, pkv_stream_t stream);
 
 /*
+ * Paged decode attention without a caller-provided workspace.  No
+ * counterpart on the pages: this entry point exists for callers that cannot
+ * allocate device memory at decode time (code running while a CUDA graph is
+ * being captured, plugins whose host framework owns all device allocations,
+ * hosts with a fixed memory budget).
+ *
+ * Same arguments, semantics and errors as pkv_paged_decode_attention, minus
+ * `workspace` / `workspace_bytes`.  The workspace is a static device array of
+ * PKV_NOALLOC_SCRATCH_BYTES that the library holds on every device that loads
+ * it, until the process exits; nothing is allocated by this call.
+ *   - Limit: if pkv_decode_workspace_bytes(...) for these sizes exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current).  Make that first call
+ *     outside any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents (each call rewrites what must start at zero before
+ *     its kernels read it).  Calls whose kernels overlap on the GPU -- on two
+ *     streams, or from two host threads without ordering -- race on it and
+ *     give wrong results; order them on one stream.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+PKV_API pkv_status pkv_paged_decode_attention_noalloc(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+    pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale, void* out, pkv_stream_t stream);
+
+/*
  * Read and clear the status word of the current device (a bit-or of
  * PKV_DEV_* flags set by kernels since the last read).  Synchronous: waits
  * for the device's work to finish.  `host_code` is a host pointer.

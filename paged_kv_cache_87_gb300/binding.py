@@ -7,7 +7,8 @@ cannot be loaded the calls raise.
 
 Functions carry the C names:
   pkv_decode_workspace_bytes, pkv_paged_decode_attention,
-  pkv_reshape_and_cache, pkv_copy_blocks, pkv_get_device_status,
+  pkv_paged_decode_attention_noalloc, pkv_reshape_and_cache, pkv_copy_blocks,
+  pkv_get_device_status,
   pkv_status_string, pkv_version.
 """
 from __future__ import annotations
@@ -35,6 +36,11 @@ _SIGNATURES = {
         [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_float, ctypes.c_void_p,
                                                      ctypes.c_size_t, ctypes.c_void_p,
+                                                     ctypes.c_void_p]),
+    "pkv_paged_decode_attention_noalloc": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_float, ctypes.c_void_p,
                                                      ctypes.c_void_p]),
     "pkv_reshape_and_cache": (
         ctypes.c_int,
@@ -152,6 +158,39 @@ def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cac
         int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
     _check("pkv_paged_decode_attention", st)
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20   # PKV_NOALLOC_SCRATCH_BYTES
+
+
+def pkv_paged_decode_attention_noalloc(query: torch.Tensor, k_cache: torch.Tensor,
+                                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                       context_lens: torch.Tensor, max_context_len: int,
+                                       scale: float, kv_scale: float = 1.0,
+                                       out: torch.Tensor | None = None,
+                                       stream=None) -> torch.Tensor:
+    """Decode with the library's static device scratch instead of a workspace.
+
+    For callers that cannot allocate device memory while they decode.  Fails
+    with PKV_ERR_WORKSPACE when the sizes need more than 16 MiB of scratch.
+    Calls that overlap on the GPU race on the shared scratch: keep them on
+    one stream.  (``out`` is allocated here only when not given.)
+    """
+    S, Hq, d = query.shape
+    NB, Hkv, B, _ = k_cache.shape
+    for t, n in ((query, "query"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens")):
+        _cuda(t, n)
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    st = load().pkv_paged_decode_attention_noalloc(
+        query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), S, Hq, Hkv, d, B, NB, block_tables.shape[1],
+        int(max_context_len), float(scale), dtype_code(query), dtype_code(k_cache),
+        float(kv_scale), out.data_ptr(), _stream_ptr(stream))
+    _check("pkv_paged_decode_attention_noalloc", st)
     return out
 
 
