@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the workload to its first N sequences (profiling captures)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -267,7 +269,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
-    w = inputs.make_config(args.workload)
+    w = inputs.make_config(args.workload, num_seqs=args.num_seqs)
     st = DeviceState(w, device)
     st.run_setup()
     stream = torch.cuda.Stream(device)
