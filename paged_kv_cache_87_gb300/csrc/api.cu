@@ -59,8 +59,9 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Work decomposition shared by pkv_decode_workspace_bytes and the decode call.
 struct Plan {
     int group, hpi, nsub;
-    int chunk_tokens, max_chunks;
-    size_t off_hdr, off_ctx, off_items, off_units, off_pm, off_pl, off_pacc, total;
+    int chunk_tokens, max_chunks, part_stride;
+    size_t off_hdr, off_ctx, off_items, off_prefix, off_workers, off_units, off_pm, off_pl,
+        off_pacc, total;
 };
 
 // Chunk length: at least 512 tokens, a multiple of 64 (every stage size and
@@ -80,13 +81,19 @@ pkv_status make_plan(int S, int Hq, int Hkv, int HD, int B, int max_ctx, Plan* p
     if (C > kMaxItemBlocks * B) return PKV_ERR_UNSUPPORTED;   // context too long
     p.chunk_tokens = C;
     p.max_chunks = max_ctx > 0 ? (max_ctx + C - 1) / C : 1;
+    // partial states per (sequence, query head): a fixed-chunk split has at most
+    // max_chunks; a balanced split (quota >= one chunk) cuts a unit into at most
+    // max_chunks + 1 segments
+    p.part_stride = p.max_chunks + 1;
     const size_t s = (size_t)S, mc = (size_t)p.max_chunks;
     size_t off = 0;
-    p.off_hdr = off;    off += 256;
-    p.off_ctx = off;    off = round_up(off + s * 4, 256);
-    p.off_items = off;  off = round_up(off + s * mc * 8, 256);
-    p.off_units = off;  off = round_up(off + s * Hkv * p.nsub * 4, 256);
-    const size_t partial_states = p.max_chunks > 1 ? s * Hq * mc : 0;
+    p.off_hdr = off;     off += 256;
+    p.off_ctx = off;     off = round_up(off + s * 4, 256);
+    p.off_items = off;   off = round_up(off + s * mc * 8, 256);
+    p.off_prefix = off;  off = round_up(off + (s + 1) * 4, 256);
+    p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 4, 256);
+    p.off_units = off;   off = round_up(off + s * Hkv * p.nsub * 4, 256);
+    const size_t partial_states = p.max_chunks > 1 ? s * Hq * (size_t)p.part_stride : 0;
     p.off_pm = off;     off = round_up(off + partial_states * 4, 256);
     p.off_pl = off;     off = round_up(off + partial_states * 4, 256);
     p.off_pacc = off;   off = round_up(off + partial_states * HD * 4, 256);
@@ -158,8 +165,11 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     p.out = out;
     p.ws.counter = reinterpret_cast<unsigned*>(ws + plan.off_hdr);
     p.ws.total = p.ws.counter + 1;
+    p.ws.quota = reinterpret_cast<int*>(p.ws.counter + 2);
     p.ws.ctx_eff = reinterpret_cast<int*>(ws + plan.off_ctx);
     p.ws.items = reinterpret_cast<int2*>(ws + plan.off_items);
+    p.ws.tile_prefix = reinterpret_cast<int*>(ws + plan.off_prefix);
+    p.ws.worker_seq = reinterpret_cast<int*>(ws + plan.off_workers);
     p.ws.unit_done = reinterpret_cast<unsigned*>(ws + plan.off_units);
     p.ws.pm = reinterpret_cast<float*>(ws + plan.off_pm);
     p.ws.pl = reinterpret_cast<float*>(ws + plan.off_pl);
@@ -177,15 +187,24 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     p.max_context_len = max_context_len;
     p.chunk_tokens = plan.chunk_tokens;
     p.max_chunks = plan.max_chunks;
+    p.part_stride = plan.part_stride;
     const bool fp8 = kv_dtype == PKV_FP8_E4M3;
     p.qk_scale_log2 = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
     p.out_scale = fp8 ? kv_scale : 1.f;
 
+    // Groups of three or more query heads with 16-bit q and K/V run on tensor
+    // cores (8 heads per item); the rest on CUDA cores (plan.hpi heads per item).
+    const bool mma = (q_dtype == PKV_F16 || q_dtype == PKV_BF16) && kv_dtype == q_dtype &&
+                     plan.group >= 3 &&
+                     (int64_t)num_blocks * num_kv_heads * block_size <= 0x7fffffffLL;
+    const int hpi = mma ? kMmaHeadsPerItem : plan.hpi;
+    p.nsub = (plan.group + hpi - 1) / hpi;   // never above plan.nsub: the workspace fits
+
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (q_dtype) {
-    case PKV_F32: err = decode_dispatch_f32(p, kv_dtype, plan.hpi, s); break;
-    case PKV_F16: err = decode_dispatch_f16(p, kv_dtype, plan.hpi, s); break;
-    default: err = decode_dispatch_bf16(p, kv_dtype, plan.hpi, s); break;
+    case PKV_F32: err = decode_dispatch_f32(p, kv_dtype, hpi, s); break;
+    case PKV_F16: err = decode_dispatch_f16(p, kv_dtype, hpi, s); break;
+    default: err = decode_dispatch_bf16(p, kv_dtype, hpi, s); break;
     }
     return cuda_status(err);
 }

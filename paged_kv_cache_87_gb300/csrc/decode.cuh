@@ -39,16 +39,22 @@ namespace pkv {
 constexpr int kMaxMergeChunks = 256;   // chunk states merged per (sequence, head)
 constexpr int kMaxItemBlocks = 64;     // table entries a producer holds per item
 constexpr float kRescaleSlack = 8.0f;  // log2-domain headroom before moving the max
+constexpr int kMmaHeadsPerItem = 8;    // query heads per item of the tensor-core variant
+constexpr int kMaxWorkers = 4096;      // CTAs of the balanced-split decode, at most
+constexpr int kTileTokens = 64;        // split granularity of the balanced split
 
 struct DecodeWork {
-    unsigned* counter;    // next work index
-    unsigned* total;      // number of work indices
+    unsigned* counter;    // next work index (dynamic items)
+    unsigned* total;      // number of work indices (dynamic items)
+    int* quota;           // tiles per worker (balanced split)
     int* ctx_eff;         // [S] context length after clamping
     int2* items;          // [S * max_chunks] (sequence, chunk)
+    int* tile_prefix;     // [S + 1] tiles of 64 tokens x units, exclusive prefix (balanced split)
+    int* worker_seq;      // [kMaxWorkers] first sequence of each worker (balanced split)
     unsigned* unit_done;  // [S * Hkv * nsub] chunks finished
-    float* pm;            // [S * Hq * max_chunks]
-    float* pl;            // [S * Hq * max_chunks]
-    float* pacc;          // [S * Hq * max_chunks * d]
+    float* pm;            // [S * Hq * part_stride]
+    float* pl;            // [S * Hq * part_stride]
+    float* pacc;          // [S * Hq * part_stride * d]
 };
 
 struct DecodeParams {
@@ -63,6 +69,8 @@ struct DecodeParams {
     int num_seqs, num_q_heads, num_kv_heads, group, nsub;
     int head_dim, block_size, num_blocks, max_blocks, max_context_len;
     int chunk_tokens, max_chunks;
+    int part_stride;      // partial states per (sequence, query head) in the workspace
+    int num_workers;      // CTAs of the balanced-split decode
     float qk_scale_log2;  // scale * log2(e) (* kv_scale for FP8)
     float out_scale;      // kv_scale for FP8, else 1
 };
@@ -185,6 +193,103 @@ __device__ __forceinline__ void merge_factor(float ma, float mb, float& fa, floa
     M = fmaxf(ma, mb);
     fa = ma == -INFINITY ? 0.f : fast_exp2(ma - M);
     fb = mb == -INFINITY ? 0.f : fast_exp2(mb - M);
+}
+
+// End of a work item, after every consumer warp has put its state in `scratch`
+// ([NCW][HPI][HD] acc, then [NCW][HPI] m, then [NCW][HPI] l; all relative to
+// the warp's own reference max, log2 domain).  Merges the warps by the
+// rescale rule; a single-chunk sequence writes `out`, otherwise the chunk's
+// state goes to the workspace and the last CTA to finish this (sequence, kv
+// head, subgroup) merges all chunks in chunk order and writes `out`.
+// Called by all NCW*32 consumer threads; leaves `scratch` free for reuse.
+template <typename QT, int HD, int HPI, int NCW>
+__device__ __forceinline__ void finish_item(const DecodeParams& p, const StageMeta& meta,
+                                            float* scratch, int* misc, int ctid) {
+    constexpr int NT = NCW * 32;
+    float* s_acc = scratch;
+    float* s_m = scratch + NCW * HPI * HD;
+    float* s_l = s_m + NCW * HPI;
+    named_bar_sync(1, NT);
+    const bool single = meta.nchunks == 1;
+    const int hq0 = meta.kvh * p.group + meta.qsub * HPI;
+    for (int idx = ctid; idx < HPI * HD; idx += NT) {
+        const int h = idx / HD, dim = idx % HD;
+        if (h >= meta.nh) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, s_m[w2 * HPI + h]);
+        float L = 0.f, A = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < NCW; ++w2) {
+            const float mw = s_m[w2 * HPI + h];
+            const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+            L = fmaf(s_l[w2 * HPI + h], f, L);
+            A = fmaf(s_acc[(w2 * HPI + h) * HD + dim], f, A);
+        }
+        const int64_t sh = (int64_t)meta.s * p.num_q_heads + hq0 + h;
+        if (single) {
+            store_from_float<QT>(p.out, sh * HD + dim, L > 0.f ? A / L * p.out_scale : 0.f);
+        } else {
+            const int64_t pi = sh * p.part_stride + meta.chunk;
+            p.ws.pacc[pi * HD + dim] = A;
+            if (dim == 0) {
+                p.ws.pm[pi] = M;
+                p.ws.pl[pi] = L;
+            }
+        }
+    }
+    named_bar_sync(1, NT);   // scratch reads done; partial stores issued by every thread
+    if (single) return;
+    if (ctid == 0) {
+        // the barrier above orders every thread's partial stores before this
+        // thread's gpu-scope fence, which publishes them before the arrival
+        __threadfence();
+        const int unit = (meta.s * p.num_kv_heads + meta.kvh) * p.nsub + meta.qsub;
+        const unsigned done = atomicAdd(&p.ws.unit_done[unit], 1u);
+        misc[0] = done == (unsigned)(meta.nchunks - 1);
+        if (misc[0]) __threadfence();
+    }
+    named_bar_sync(1, NT);
+    if (misc[0]) {
+        // last chunk of this (sequence, kv head, subgroup) to finish: merge all chunks
+        const int nc = meta.nchunks;
+        float* f_tab = scratch;                        // [HPI][kMaxMergeChunks] factors
+        float* lsum = scratch + HPI * kMaxMergeChunks; // [HPI] merged l
+        for (int idx = ctid; idx < HPI * nc; idx += NT) {
+            const int h = idx / nc, c = idx % nc;
+            if (h >= meta.nh) continue;
+            const int64_t pi = ((int64_t)meta.s * p.num_q_heads + hq0 + h) * p.part_stride + c;
+            f_tab[h * kMaxMergeChunks + c] = __ldcg(&p.ws.pm[pi]);
+        }
+        named_bar_sync(1, NT);
+        if (ctid < HPI && ctid < meta.nh) {
+            const int h = ctid;
+            float M = -INFINITY;
+            for (int c = 0; c < nc; ++c) M = fmaxf(M, f_tab[h * kMaxMergeChunks + c]);
+            float L = 0.f;
+            for (int c = 0; c < nc; ++c) {
+                const int64_t pi = ((int64_t)meta.s * p.num_q_heads + hq0 + h) * p.part_stride + c;
+                const float mc = f_tab[h * kMaxMergeChunks + c];
+                const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
+                f_tab[h * kMaxMergeChunks + c] = f;
+                L = fmaf(__ldcg(&p.ws.pl[pi]), f, L);
+            }
+            lsum[h] = L;
+        }
+        named_bar_sync(1, NT);
+        for (int idx = ctid; idx < HPI * HD; idx += NT) {
+            const int h = idx / HD, dim = idx % HD;
+            if (h >= meta.nh) continue;
+            const int64_t sh = (int64_t)meta.s * p.num_q_heads + hq0 + h;
+            float A = 0.f;
+            for (int c = 0; c < nc; ++c)
+                A = fmaf(__ldcg(&p.ws.pacc[(sh * p.part_stride + c) * HD + dim]),
+                         f_tab[h * kMaxMergeChunks + c], A);
+            const float L = lsum[h];
+            store_from_float<QT>(p.out, sh * HD + dim, L > 0.f ? A / L * p.out_scale : 0.f);
+        }
+    }
+    named_bar_sync(1, NT);   // scratch and misc are reused by the next item
 }
 
 template <typename QT, typename KT, int HD, int HPI>
@@ -466,90 +571,7 @@ __global__ void __launch_bounds__(SimtCfg<QT, KT, HD, HPI>::THREADS, 2)
                 }
             }
         }
-        named_bar_sync(1, NCW * 32);
-        const bool single = meta.nchunks == 1;
-        const int hq0 = meta.kvh * p.group + meta.qsub * HPI;
-        for (int idx = ctid; idx < HPI * HD; idx += NCW * 32) {
-            const int h = idx / HD, dim = idx % HD;
-            if (h >= meta.nh) continue;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) M = fmaxf(M, s_m[w2 * HPI + h]);
-            float L = 0.f, A = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) {
-                const float mw = s_m[w2 * HPI + h];
-                const float f = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
-                L = fmaf(s_l[w2 * HPI + h], f, L);
-                A = fmaf(s_acc[(w2 * HPI + h) * HD + dim], f, A);
-            }
-            const int64_t sh = (int64_t)meta.s * p.num_q_heads + hq0 + h;
-            if (single) {
-                store_from_float<QT>(p.out, sh * HD + dim, L > 0.f ? A / L * p.out_scale : 0.f);
-            } else {
-                const int64_t pi = sh * p.max_chunks + meta.chunk;
-                p.ws.pacc[pi * HD + dim] = A;
-                if (dim == 0) {
-                    p.ws.pm[pi] = M;
-                    p.ws.pl[pi] = L;
-                }
-            }
-        }
-        if (single) {
-            named_bar_sync(1, NCW * 32);   // scratch is reused by the next item
-            continue;
-        }
-        __threadfence();
-        named_bar_sync(1, NCW * 32);
-        if (ctid == 0) {
-            const int unit = (meta.s * p.num_kv_heads + meta.kvh) * p.nsub + meta.qsub;
-            const unsigned done = atomicAdd(&p.ws.unit_done[unit], 1u);
-            misc[0] = done == (unsigned)(meta.nchunks - 1);
-        }
-        named_bar_sync(1, NCW * 32);
-        if (misc[0]) {
-            // last chunk of this (sequence, kv head, subgroup) to finish: merge all chunks
-            __threadfence();
-            const int nc = meta.nchunks;
-            float* f_tab = scratch;                        // [HPI][nc] rescale factors
-            float* lsum = scratch + HPI * kMaxMergeChunks; // [HPI] merged l
-            for (int idx = ctid; idx < HPI * nc; idx += NCW * 32) {
-                const int h = idx / nc, c = idx % nc;
-                if (h >= meta.nh) continue;
-                const int64_t pi =
-                    ((int64_t)meta.s * p.num_q_heads + hq0 + h) * p.max_chunks + c;
-                f_tab[h * kMaxMergeChunks + c] = __ldcg(&p.ws.pm[pi]);
-            }
-            named_bar_sync(1, NCW * 32);
-            if (ctid < HPI && ctid < meta.nh) {
-                const int h = ctid;
-                float M = -INFINITY;
-                for (int c = 0; c < nc; ++c) M = fmaxf(M, f_tab[h * kMaxMergeChunks + c]);
-                float L = 0.f;
-                for (int c = 0; c < nc; ++c) {
-                    const int64_t pi =
-                        ((int64_t)meta.s * p.num_q_heads + hq0 + h) * p.max_chunks + c;
-                    const float mc = f_tab[h * kMaxMergeChunks + c];
-                    const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
-                    f_tab[h * kMaxMergeChunks + c] = f;
-                    L = fmaf(__ldcg(&p.ws.pl[pi]), f, L);
-                }
-                lsum[h] = L;
-            }
-            named_bar_sync(1, NCW * 32);
-            for (int idx = ctid; idx < HPI * HD; idx += NCW * 32) {
-                const int h = idx / HD, dim = idx % HD;
-                if (h >= meta.nh) continue;
-                const int64_t sh = (int64_t)meta.s * p.num_q_heads + hq0 + h;
-                float A = 0.f;
-                for (int c = 0; c < nc; ++c)
-                    A = fmaf(__ldcg(&p.ws.pacc[(sh * p.max_chunks + c) * HD + dim]),
-                             f_tab[h * kMaxMergeChunks + c], A);
-                const float L = lsum[h];
-                store_from_float<QT>(p.out, sh * HD + dim, L > 0.f ? A / L * p.out_scale : 0.f);
-            }
-        }
-        named_bar_sync(1, NCW * 32);
+        finish_item<QT, HD, HPI, NCW>(p, meta, scratch, misc, ctid);
     }
 }
 

@@ -4,7 +4,11 @@
 // compile in parallel translation units.
 #pragma once
 
+#include <type_traits>
+
 #include "decode.cuh"
+#include "decode_mma.cuh"
+#include "tmap.cuh"
 
 namespace pkv {
 
@@ -40,8 +44,49 @@ cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Grouped-head variant on tensor cores: 16-bit q and K/V, 8 query heads per item.
+template <typename QT, int HD>
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+    using Cfg = MmaCfg<QT, HD>;
+    static OccCache occ;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kernel = decode_mma_kernel<QT, HD>;
+    if (occ.ctas[dev] == 0) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)Cfg::SMEM);
+        if (err != cudaSuccess) return err;
+        int per_sm = 0, sms = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, Cfg::THREADS,
+                                                            Cfg::SMEM);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        occ.ctas[dev] = min((per_sm > 0 ? per_sm : 1) * sms, kMaxWorkers);
+    }
+    CUtensorMap tk, tv;
+    const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    if (!encode_pool_map(&tk, p.k_cache, HD, 2, rows, p.block_size) ||
+        !encode_pool_map(&tv, p.v_cache, HD, 2, rows, p.block_size))
+        return cudaErrorInvalidValue;
+    DecodeParams ps = p;
+    ps.num_workers = occ.ctas[dev];
+    plan_split_kernel<QT><<<1, 1024, 0, stream>>>(ps);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    kernel<<<ps.num_workers, Cfg::THREADS, Cfg::SMEM, stream>>>(ps, tk, tv);
+    return cudaGetLastError();
+}
+
 template <typename QT, typename KT>
 cudaError_t dispatch_decode_kv(const DecodeParams& p, int hpi, cudaStream_t stream) {
+    if constexpr (std::is_same<QT, KT>::value && !std::is_same<QT, F32>::value) {
+        if (hpi == kMmaHeadsPerItem)
+            return p.head_dim == 128 ? launch_decode_mma<QT, 128>(p, stream)
+                                     : launch_decode_mma<QT, 64>(p, stream);
+    }
     if (p.head_dim == 128) {
         if (hpi == 1) return launch_decode_simt<QT, KT, 128, 1>(p, stream);
         if (hpi == 2) return launch_decode_simt<QT, KT, 128, 2>(p, stream);
