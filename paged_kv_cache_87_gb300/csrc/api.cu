@@ -192,10 +192,11 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     p.qk_scale_log2 = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
     p.out_scale = fp8 ? kv_scale : 1.f;
 
-    // Groups of three or more query heads with 16-bit q and K/V run on tensor
-    // cores (8 heads per item); the rest on CUDA cores (plan.hpi heads per item).
-    const bool mma = (q_dtype == PKV_F16 || q_dtype == PKV_BF16) && kv_dtype == q_dtype &&
-                     plan.group >= 3 &&
+    // 16-bit q with 16-bit K/V (any head_dim) or FP8 K/V (head_dim 128) run on
+    // tensor cores, 8 query heads per item; fp32 and the rest on CUDA cores
+    // (plan.hpi heads per item).
+    const bool mma = (q_dtype == PKV_F16 || q_dtype == PKV_BF16) &&
+                     (kv_dtype == q_dtype || (kv_dtype == PKV_FP8_E4M3 && head_dim == 128)) &&
                      (int64_t)num_blocks * num_kv_heads * block_size <= 0x7fffffffLL;
     const int hpi = mma ? kMmaHeadsPerItem : plan.hpi;
     p.nsub = (plan.group + hpi - 1) / hpi;   // never above plan.nsub: the workspace fits

@@ -44,16 +44,16 @@ cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Grouped-head variant on tensor cores: 16-bit q and K/V, 8 query heads per item.
-template <typename QT, int HD>
+// Tensor-core variant: 16-bit q, 16-bit or FP8 K/V, 8 query heads per item.
+template <typename QT, typename KT, int HD>
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
-    using Cfg = MmaCfg<QT, HD>;
+    using Cfg = MmaCfg<QT, KT, HD>;
     static OccCache occ;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kernel = decode_mma_kernel<QT, HD>;
+    auto kernel = decode_mma_kernel<QT, KT, HD>;
     if (occ.ctas[dev] == 0) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)Cfg::SMEM);
@@ -68,8 +68,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
     }
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
-    if (!encode_pool_map(&tk, p.k_cache, HD, 2, rows, p.block_size) ||
-        !encode_pool_map(&tv, p.v_cache, HD, 2, rows, p.block_size))
+    if (!encode_pool_map(&tk, p.k_cache, HD, KT::bytes, rows, p.block_size) ||
+        !encode_pool_map(&tv, p.v_cache, HD, KT::bytes, rows, p.block_size))
         return cudaErrorInvalidValue;
     DecodeParams ps = p;
     ps.num_workers = occ.ctas[dev];
@@ -82,10 +82,14 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
 
 template <typename QT, typename KT>
 cudaError_t dispatch_decode_kv(const DecodeParams& p, int hpi, cudaStream_t stream) {
-    if constexpr (std::is_same<QT, KT>::value && !std::is_same<QT, F32>::value) {
-        if (hpi == kMmaHeadsPerItem)
-            return p.head_dim == 128 ? launch_decode_mma<QT, 128>(p, stream)
-                                     : launch_decode_mma<QT, 64>(p, stream);
+    if constexpr (!std::is_same<QT, F32>::value) {
+        if (hpi == kMmaHeadsPerItem) {
+            if constexpr (std::is_same<KT, E4M3>::value)
+                return launch_decode_mma<QT, KT, 128>(p, stream);
+            else
+                return p.head_dim == 128 ? launch_decode_mma<QT, KT, 128>(p, stream)
+                                         : launch_decode_mma<QT, KT, 64>(p, stream);
+        }
     }
     if (p.head_dim == 128) {
         if (hpi == 1) return launch_decode_simt<QT, KT, 128, 1>(p, stream);

@@ -34,6 +34,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "decode.cuh"
 
 namespace pkv {
@@ -121,24 +123,49 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ------------------------------------------------------------------ config --
 
-template <typename QT, int HD>
+template <typename QT, typename KT, int HD>
 struct MmaCfg {
+    static constexpr bool FP8 = std::is_same<KT, E4M3>::value;
+    using MT = typename std::conditional<FP8, F16, KT>::type;   // mma operand type
     static constexpr int HPI = kMmaHeadsPerItem;  // query heads per item (mma N = 8)
     static constexpr int TPS = 32;                // tokens per stage: two 16-token m-tiles
-    static constexpr int HALVES = HD / 64;        // 128-byte column halves of a row
+    static constexpr int ROWB = HD * KT::bytes;   // bytes of one K/V row
+    static constexpr int HALVES = ROWB / 128;     // 128-byte column slices of a row
+    static constexpr int ELEMS_PER_SLICE = 128 / KT::bytes;
     static constexpr int KSTEPS = HD / 16;        // mma k-steps of Q.K^T
     static constexpr int MTILES = HD / 16;        // mma m-tiles of P.V (over d)
-    static constexpr int HALF_BYTES = TPS * 128;  // one 64-column half of a stage
+    static constexpr int HALF_BYTES = TPS * 128;  // one 128-byte slice of a stage
     static constexpr int KV_BYTES = HALVES * HALF_BYTES;
     static constexpr int Q_BYTES = HPI * HD * 2;
     static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 1023) / 1024 * 1024;
-    static constexpr int NSTAGE = HD == 128 ? 3 : 5;
+    static constexpr int NSTAGE = FP8 ? 5 : (HD == 128 ? 3 : 5);
     static constexpr int THREADS = 64;            // consumer warp + producer warp
     static constexpr size_t OFF_METAS = (size_t)NSTAGE * STAGE_BYTES;
     static constexpr size_t OFF_BARS = OFF_METAS + NSTAGE * sizeof(StageMeta);
     static constexpr size_t SMEM = OFF_BARS + 2 * NSTAGE * sizeof(uint64_t) + 1024;
     static_assert(HD == 64 || HD == 128, "head_dim");
+    static_assert(!FP8 || HD == 128, "FP8 rows must be 128 bytes");
+    static_assert(std::is_same<QT, F16>::value || std::is_same<QT, BF16>::value, "q type");
 };
+
+// Two e4m3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes),
+                                               __NV_E4M3);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two 16-bit q values (low first) as the mma operand type MT.
+template <typename QT, typename MT>
+__device__ __forceinline__ uint32_t q_pair(uint32_t raw) {
+    if constexpr (std::is_same<QT, MT>::value) {
+        return raw;
+    } else {   // bf16 q with an f16 mma (FP8 KV): exact for |q| in f16's normal range
+        __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&raw);
+        __half2 h = __floats2half2_rn(__low2float(b), __high2float(b));
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `r` in a 128-byte-row,
 // 128-byte-swizzled region whose base is 1024-byte aligned.
@@ -301,11 +328,12 @@ __device__ __forceinline__ Window make_window(const DecodeParams& p, int worker,
     return w;
 }
 
-template <typename QT, int HD>
-__global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
+template <typename QT, typename KT, int HD>
+__global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                                         const __grid_constant__ CUtensorMap tmK,
                                                         const __grid_constant__ CUtensorMap tmV) {
-    using Cfg = MmaCfg<QT, HD>;
+    using Cfg = MmaCfg<QT, KT, HD>;
+    using MT = typename Cfg::MT;
     constexpr int HPI = Cfg::HPI, TPS = Cfg::TPS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -388,7 +416,7 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
                     m.flags = (qstage ? kFirst : 0) |
                               (win.last && st == nstages - 1 ? kLast : 0);
                     mbar_arrive_expect_tx(&full[stage],
-                                          2u * (uint32_t)(nblk * B) * (HD * 2) + qbytes);
+                                          2u * (uint32_t)(nblk * B) * Cfg::ROWB + qbytes);
                 }
                 __syncwarp();
                 const int rel = fb + lane - jb0;
@@ -400,10 +428,11 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
                     const int row0 = lane * B;                       // stage row of the block
 #pragma unroll
                     for (int h = 0; h < Cfg::HALVES; ++h) {
-                        tma_load_2d(sbase + h * Cfg::HALF_BYTES + row0 * 128, &tmK, h * 64, y,
+                        const int x = h * Cfg::ELEMS_PER_SLICE;
+                        tma_load_2d(sbase + h * Cfg::HALF_BYTES + row0 * 128, &tmK, x, y,
                                     &full[stage], policy);
                         tma_load_2d(sbase + Cfg::KV_BYTES + h * Cfg::HALF_BYTES + row0 * 128,
-                                    &tmV, h * 64, y, &full[stage], policy);
+                                    &tmV, x, y, &full[stage], policy);
                     }
                 }
                 if (qstage && lane == 31) {
@@ -435,10 +464,15 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
     // ========================= consumer warp =========================
     const int g = lane >> 2, c = lane & 3;
     uint32_t qf[Cfg::KSTEPS][2];      // Q^T B fragments
-    float o[Cfg::MTILES][4];          // O^T C fragments: (d = 16mt + g [+8], heads 2c, 2c+1)
+    float o[Cfg::MTILES][4];          // O^T C fragments, rows mapped to d by d_row()
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int stage = 0;
     uint32_t phase = 0;
+    // d index of C-fragment row g (half 0) or g + 8 (half 1) of P.V m-tile mt
+    auto d_row = [&](int mt, int half) -> int {
+        if constexpr (Cfg::FP8) return 32 * (mt >> 1) + 2 * g + (mt & 1) + 16 * half;
+        else return 16 * mt + g + 8 * half;
+    };
 
     while (true) {
         if (!mbar_wait(&full[stage], phase)) {
@@ -456,8 +490,14 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
             const bool live = g < meta.nh;
 #pragma unroll
             for (int t = 0; t < Cfg::KSTEPS; ++t) {
-                qf[t][0] = live ? sQ[(g * HD + 16 * t + 2 * c) >> 1] : 0u;
-                qf[t][1] = live ? sQ[(g * HD + 16 * t + 8 + 2 * c) >> 1] : 0u;
+                if constexpr (Cfg::FP8) {
+                    // k-slots (2c, 2c+1) <-> dims 16t+4c, +1; (8+2c, 9+2c) <-> 16t+4c+2, +3
+                    qf[t][0] = live ? q_pair<QT, MT>(sQ[(g * HD + 16 * t + 4 * c) >> 1]) : 0u;
+                    qf[t][1] = live ? q_pair<QT, MT>(sQ[(g * HD + 16 * t + 4 * c + 2) >> 1]) : 0u;
+                } else {
+                    qf[t][0] = live ? sQ[(g * HD + 16 * t + 2 * c) >> 1] : 0u;
+                    qf[t][1] = live ? sQ[(g * HD + 16 * t + 8 + 2 * c) >> 1] : 0u;
+                }
             }
 #pragma unroll
             for (int mt = 0; mt < Cfg::MTILES; ++mt)
@@ -485,17 +525,41 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
         float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         {
             const int rl = (lane & 7) + ((lane >> 3) & 1) * 8;
+            if constexpr (Cfg::FP8) {
+                // one 16-byte chunk = 16 e4m3 dims = one k-step; a lane's 4 bytes of a
+                // row feed its k-slots (2c, 2c+1) and (8+2c, 9+2c)
 #pragma unroll
-            for (int t = 0; t < Cfg::KSTEPS; ++t) {
-                const int half = t >> 2, chunk = (t & 3) * 2 + (lane >> 4);
-                const uint32_t base = sK + half * Cfg::HALF_BYTES;
-                uint32_t a[4];
-                ldsm_x4(base + swz(rl, chunk), a);
-                Mma<QT>::run(sa[0], a, qf[t][0], qf[t][1]);
-                if (two) {
-                    uint32_t b[4];
-                    ldsm_x4(base + swz(16 + rl, chunk), b);
-                    Mma<QT>::run(sa[1], b, qf[t][0], qf[t][1]);
+                for (int pr = 0; pr < Cfg::KSTEPS / 2; ++pr) {
+                    const int chunk = 2 * pr + (lane >> 4);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        if (mt == 1 && !two) break;
+                        uint32_t r[4];
+                        ldsm_x4(sK + swz(16 * mt + rl, chunk), r);
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const uint32_t lo = r[2 * k], hi = r[2 * k + 1];
+                            const uint32_t a[4] = {e4m3x2_to_f16x2(lo & 0xffffu),
+                                                   e4m3x2_to_f16x2(hi & 0xffffu),
+                                                   e4m3x2_to_f16x2(lo >> 16),
+                                                   e4m3x2_to_f16x2(hi >> 16)};
+                            Mma<MT>::run(sa[mt], a, qf[2 * pr + k][0], qf[2 * pr + k][1]);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < Cfg::KSTEPS; ++t) {
+                    const int half = t >> 2, chunk = (t & 3) * 2 + (lane >> 4);
+                    const uint32_t base = sK + half * Cfg::HALF_BYTES;
+                    uint32_t a[4];
+                    ldsm_x4(base + swz(rl, chunk), a);
+                    Mma<MT>::run(sa[0], a, qf[t][0], qf[t][1]);
+                    if (two) {
+                        uint32_t b[4];
+                        ldsm_x4(base + swz(16 + rl, chunk), b);
+                        Mma<MT>::run(sa[1], b, qf[t][0], qf[t][1]);
+                    }
                 }
             }
         }
@@ -537,9 +601,9 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
         for (int mt = 0; mt < 2; ++mt) {
             float f0, f1, f2, f3;
             const uint32_t p01 =
-                Mma<QT>::pack(fast_exp2(x[mt][0] - m0), fast_exp2(x[mt][1] - m1), f0, f1);
+                Mma<MT>::pack(fast_exp2(x[mt][0] - m0), fast_exp2(x[mt][1] - m1), f0, f1);
             const uint32_t p23 =
-                Mma<QT>::pack(fast_exp2(x[mt][2] - m0), fast_exp2(x[mt][3] - m1), f2, f3);
+                Mma<MT>::pack(fast_exp2(x[mt][2] - m0), fast_exp2(x[mt][3] - m1), f2, f3);
             l0 += f0 + f2;
             l1 += f1 + f3;
             pb[mt][0] = movmatrix_trans(p01);
@@ -549,17 +613,41 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
         {
             const int mi = lane >> 3;
             const int rv = (lane & 7) + (mi >> 1) * 8;
+            if constexpr (Cfg::FP8) {
+                // a transposed 8x8 b16 block of e4m3 rows gives each lane V[2c][2g, 2g+1]
+                // and V[2c+1][2g, 2g+1]; byte permutes split them into an even-d and an
+                // odd-d A fragment (m-tiles 2pr and 2pr+1 over dims 32pr .. 32pr+31)
 #pragma unroll
-            for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-                const int half = mt >> 2, chunk = (mt & 3) * 2 + (mi & 1);
-                const uint32_t base = sV + half * Cfg::HALF_BYTES;
-                uint32_t a[4];
-                ldsm_x4_trans(base + swz(rv, chunk), a);
-                Mma<QT>::run(o[mt], a, pb[0][0], pb[0][1]);
-                if (two) {
-                    uint32_t b[4];
-                    ldsm_x4_trans(base + swz(16 + rv, chunk), b);
-                    Mma<QT>::run(o[mt], b, pb[1][0], pb[1][1]);
+                for (int pr = 0; pr < Cfg::MTILES / 2; ++pr) {
+                    const int chunk = 2 * pr + (mi & 1);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        if (ks == 1 && !two) break;
+                        uint32_t r[4];
+                        ldsm_x4_trans(sV + swz(16 * ks + rv, chunk), r);
+                        uint32_t ev[4], od[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            ev[k] = e4m3x2_to_f16x2(__byte_perm(r[k], 0u, 0x0020));
+                            od[k] = e4m3x2_to_f16x2(__byte_perm(r[k], 0u, 0x0031));
+                        }
+                        Mma<MT>::run(o[2 * pr], ev, pb[ks][0], pb[ks][1]);
+                        Mma<MT>::run(o[2 * pr + 1], od, pb[ks][0], pb[ks][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < Cfg::MTILES; ++mt) {
+                    const int half = mt >> 2, chunk = (mt & 3) * 2 + (mi & 1);
+                    const uint32_t base = sV + half * Cfg::HALF_BYTES;
+                    uint32_t a[4];
+                    ldsm_x4_trans(base + swz(rv, chunk), a);
+                    Mma<MT>::run(o[mt], a, pb[0][0], pb[0][1]);
+                    if (two) {
+                        uint32_t b[4];
+                        ldsm_x4_trans(base + swz(16 + rv, chunk), b);
+                        Mma<MT>::run(o[mt], b, pb[1][0], pb[1][1]);
+                    }
                 }
             }
         }
@@ -584,14 +672,14 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
             const float ib = l1 > 0.f ? p.out_scale / l1 : 0.f;
 #pragma unroll
             for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-                const int d = 16 * mt + g;
+                const int d0 = d_row(mt, 0), d1 = d_row(mt, 1);
                 if (ha < meta.nh) {
-                    store_from_float<QT>(p.out, sha * HD + d, o[mt][0] * ia);
-                    store_from_float<QT>(p.out, sha * HD + d + 8, o[mt][2] * ia);
+                    store_from_float<QT>(p.out, sha * HD + d0, o[mt][0] * ia);
+                    store_from_float<QT>(p.out, sha * HD + d1, o[mt][2] * ia);
                 }
                 if (hb < meta.nh) {
-                    store_from_float<QT>(p.out, shb * HD + d, o[mt][1] * ib);
-                    store_from_float<QT>(p.out, shb * HD + d + 8, o[mt][3] * ib);
+                    store_from_float<QT>(p.out, shb * HD + d0, o[mt][1] * ib);
+                    store_from_float<QT>(p.out, shb * HD + d1, o[mt][3] * ib);
                 }
             }
             continue;
@@ -600,14 +688,14 @@ __global__ void __launch_bounds__(64) decode_mma_kernel(DecodeParams p,
         const int64_t pb_i = shb * p.part_stride + meta.chunk;
 #pragma unroll
         for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-            const int d = 16 * mt + g;
+            const int d0 = d_row(mt, 0), d1 = d_row(mt, 1);
             if (ha < meta.nh) {
-                p.ws.pacc[pa_i * HD + d] = o[mt][0];
-                p.ws.pacc[pa_i * HD + d + 8] = o[mt][2];
+                p.ws.pacc[pa_i * HD + d0] = o[mt][0];
+                p.ws.pacc[pa_i * HD + d1] = o[mt][2];
             }
             if (hb < meta.nh) {
-                p.ws.pacc[pb_i * HD + d] = o[mt][1];
-                p.ws.pacc[pb_i * HD + d + 8] = o[mt][3];
+                p.ws.pacc[pb_i * HD + d0] = o[mt][1];
+                p.ws.pacc[pb_i * HD + d1] = o[mt][3];
             }
         }
         if (g == 0) {
