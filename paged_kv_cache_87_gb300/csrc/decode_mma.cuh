@@ -299,32 +299,45 @@ struct Window {
     int first, last;            // first / last window of the segment
 };
 
+// The sequence a producer is currently walking: its tile range [lo, hi) in
+// the flattened (unit, tile) order and its context length.
+struct SeqCursor {
+    int s, lo, hi, ctx;
+};
+
+__device__ __forceinline__ void seq_load(const DecodeParams& p, SeqCursor& sc) {
+    sc.lo = __ldcg(&p.ws.tile_prefix[sc.s]);
+    sc.hi = __ldcg(&p.ws.tile_prefix[sc.s + 1]);
+    sc.ctx = __ldcg(&p.ws.ctx_eff[sc.s]);
+}
+
 // The window starting at flattened tile `pos` of a worker whose range is
-// [a, end); `s` is advanced in place to the sequence holding `pos`.
+// [a, end); `sc` advances in place to the sequence holding `pos` (global
+// loads only when the sequence changes).
 __device__ __forceinline__ Window make_window(const DecodeParams& p, int worker, int a, int end,
-                                              int q, int pos, int& s) {
+                                              int q, int pos, SeqCursor& sc) {
     Window w{};
     if (pos >= end) return w;
-    while (__ldcg(&p.ws.tile_prefix[s + 1]) <= pos) ++s;
-    const int upi = p.num_kv_heads * p.nsub;
-    const int ctx = __ldcg(&p.ws.ctx_eff[s]);
-    const int tiles = (ctx + kTileTokens - 1) / kTileTokens;
-    const int rel = pos - __ldcg(&p.ws.tile_prefix[s]);
+    while (sc.hi <= pos) {
+        ++sc.s;
+        seq_load(p, sc);
+    }
+    const int tiles = (sc.ctx + kTileTokens - 1) / kTileTokens;
+    const int rel = pos - sc.lo;
     const int u = rel / tiles, tile = rel % tiles;
     const int ustart = pos - tile, uend = ustart + tiles;
     const int wt = min(min(p.block_size, uend - pos), end - pos);   // <= 64 blocks
     w.valid = 1;
-    w.s = s;
+    w.s = sc.s;
     w.kvh = u / p.nsub;
     w.qsub = u % p.nsub;
     w.nh = min(kMmaHeadsPerItem, p.group - w.qsub * kMmaHeadsPerItem);
     w.seg = worker - ustart / q;
     w.nseg = (uend - 1) / q - ustart / q + 1;
     w.t0 = tile * kTileTokens;
-    w.t1 = min((tile + wt) * kTileTokens, ctx);
+    w.t1 = min((tile + wt) * kTileTokens, sc.ctx);
     w.first = pos == a || pos == ustart;
     w.last = pos + wt == end || pos + wt == uend;
-    (void)upi;
     return w;
 }
 
@@ -367,8 +380,9 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        int s = a < end ? p.ws.worker_seq[blockIdx.x] : 0;
-        Window win = make_window(p, blockIdx.x, a, end, q, a, s);
+        SeqCursor sc{a < end ? p.ws.worker_seq[blockIdx.x] : 0, 0, 0, 0};
+        if (a < end) seq_load(p, sc);
+        Window win = make_window(p, blockIdx.x, a, end, q, a, sc);
         int pos = a;
         int e0 = 0, e1 = 0;
         if (win.valid) {
@@ -378,17 +392,9 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
             e1 = lane + 32 < nb ? trow[jb0 + lane + 32] : 0;
         }
         while (win.valid && ok) {
-            // look one window ahead: its table entries load while this one streams
             const int wtiles = (win.t1 - win.t0 + kTileTokens - 1) / kTileTokens;
-            int sn = s;
-            const Window nxt = make_window(p, blockIdx.x, a, end, q, pos + wtiles, sn);
+            Window nxt{};
             int n0 = 0, n1 = 0;
-            if (nxt.valid) {
-                const int32_t* trow = p.block_tables + (int64_t)nxt.s * p.max_blocks;
-                const int jb0 = nxt.t0 / B, nb = (nxt.t1 + B - 1) / B - jb0;
-                n0 = lane < nb ? trow[jb0 + lane] : 0;
-                n1 = lane + 32 < nb ? trow[jb0 + lane + 32] : 0;
-            }
             const int jb0 = win.t0 / B, nb = (win.t1 + B - 1) / B - jb0;
             if ((lane < nb && (e0 < 0 || e0 >= p.num_blocks)) ||
                 (lane + 32 < nb && (e1 < 0 || e1 >= p.num_blocks))) {
@@ -441,9 +447,19 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                              &full[stage]);
                 }
                 if (++stage == Cfg::NSTAGE) { stage = 0; phase ^= 1u; }
+                if (st == 0) {
+                    // look one window ahead once this window's first stage is in flight:
+                    // its block-table entries load while this window streams
+                    nxt = make_window(p, blockIdx.x, a, end, q, pos + wtiles, sc);
+                    if (nxt.valid) {
+                        const int32_t* trow = p.block_tables + (int64_t)nxt.s * p.max_blocks;
+                        const int nj0 = nxt.t0 / B, nnb = (nxt.t1 + B - 1) / B - nj0;
+                        n0 = lane < nnb ? trow[nj0 + lane] : 0;
+                        n1 = lane + 32 < nnb ? trow[nj0 + lane + 32] : 0;
+                    }
+                }
             }
             pos += wtiles;
-            s = sn;
             win = nxt;
             e0 = n0;
             e1 = n1;
