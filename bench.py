@@ -34,8 +34,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak); µs per decode step"
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ["common.cuh", "decode.cuh", "decode_launch.cuh", "decode_f32.cu",
-                  "decode_f16.cu", "decode_bf16.cu", "api.cu"]
+DECODE_SOURCES = ["common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh",
+                  "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "tmap.cu", "tmap.cuh",
+                  "api.cu"]
 
 
 def parse_args(argv=None):
@@ -367,7 +368,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(args.workload),
-                     "kernel": "plan + decode_simt (events around the decode call)",
+                     "kernel": "planning + decode kernels (CUDA events around the decode call)",
                      "decode_us": round(dec_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 5)},
