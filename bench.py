@@ -219,18 +219,19 @@ def recorded_traffic(workload: int):
 
 # ------------------------------------------------------------ CPU baseline --
 
-def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int = 0):
+def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int = 0,
+                    caches=None):
     """Time the fp64 oracle on whole (sequence, kv head) units of the workload.
 
     Returns (GB/s of KV read, seconds, bytes, threads, description).  The
-    sample's pool is built by the oracle's own reshape_and_cache / copy_blocks.
+    sample's pool is built (untimed) by the oracle's own reshape_and_cache /
+    copy_blocks, or taken from `caches`.
     """
-    import oracle
     from tests.helpers import oracle_caches, oracle_decode
     nthreads = nthreads or os.cpu_count() or 1
     G = w.num_q_heads // w.num_kv_heads
     e = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[w.kv_dtype]
-    kc, vc = oracle_caches(w)
+    kc, vc = caches if caches is not None else oracle_caches(w)
     rng = np.random.default_rng(seed)
     order = rng.permutation(w.num_seqs)
     # calibrate on one sequence's kv head 0 group
@@ -392,11 +393,13 @@ def run_reference(args, rank, world, local):
     from paged_kv_cache_87_gb300 import inputs
     import oracle
     oracle.build()
-    w = inputs.make_config(args.workload)
+    from tests.helpers import oracle_caches
+    w = inputs.make_config(args.workload, num_seqs=args.num_seqs)
+    caches = oracle_caches(w)
     per_step = max(0.2, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
     vals, secs, desc, threads = [], [], "", 1
     for i in range(args.warmup + args.steps):
-        v, s, _, threads, desc = oracle_baseline(w, per_step, seed=i)
+        v, s, _, threads, desc = oracle_baseline(w, per_step, seed=i, caches=caches)
         if i >= args.warmup:
             vals.append(v)
             secs.append(s)
