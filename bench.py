@@ -49,6 +49,8 @@ def parse_args(argv=None):
                     help="shrink the workload to its first N sequences (profiling captures)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swap", action="store_true",
+                    help="measure pkv_swap_blocks (device pool <-> pinned host pool) instead")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     return ap.parse_args(argv)
@@ -420,12 +422,55 @@ def run_reference(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args, rank, world, local):
+    """Swap bandwidth: the workload's used blocks out to pinned host memory and back."""
+    import torch
+    from paged_kv_cache_87_gb300 import binding, build, inputs
+    from paged_kv_cache_87_gb300.session import DeviceState
+    build.build()
+    torch.cuda.set_device(local)
+    w = inputs.make_config(args.workload, num_seqs=args.num_seqs)
+    st = DeviceState(w, torch.device("cuda", local))
+    st.run_setup()
+    used = np.unique(w.block_tables[w.block_tables >= 0])
+    hk = torch.empty((len(used),) + tuple(st.k_cache.shape[1:]), dtype=st.k_cache.dtype
+                     ).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([used, np.arange(len(used))], 1).astype(np.int32)
+                                 ).cuda()
+    in_pairs = torch.from_numpy(np.stack([np.arange(len(used)), used], 1).astype(np.int32)
+                                ).cuda()
+    nbytes = 2 * len(used) * st.k_cache[0].numel() * st.k_cache.element_size()
+    stream = torch.cuda.Stream()
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, args_ in (("swap_out_gbs", (st.k_cache, st.v_cache, hk, hv, out_pairs)),
+                            ("swap_in_gbs", (hk, hv, st.k_cache, st.v_cache, in_pairs))):
+            for _ in range(args.warmup):
+                binding.pkv_swap_blocks(*args_, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                binding.pkv_swap_blocks(*args_, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            res[name] = round(nbytes * args.steps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    assert binding.pkv_get_device_status() == 0
+    if rank == 0:
+        print(json.dumps({"metric": "pkv_swap_blocks bandwidth (device pool <-> pinned host)",
+                          "unit": "GB/s", **res, "bytes_per_call": nbytes,
+                          "blocks": int(len(used)), "steps": args.steps,
+                          "config": {"workload": w.name}}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
-    if args.impl == "reference":
+    if args.swap:
+        run_swap(args, rank, world, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)

@@ -63,7 +63,8 @@ typedef enum pkv_status {
     PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad scale */
     PKV_ERR_UNSUPPORTED = 2,   /* head_dim, block_size or dtype combination not built */
     PKV_ERR_WORKSPACE = 3,     /* decode workspace too small or misaligned */
-    PKV_ERR_CUDA = 4           /* a CUDA runtime call or launch failed */
+    PKV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_OUT_OF_BLOCKS = 5  /* block manager: the free list cannot satisfy the request */
 } pkv_status;
 
 /* Bits of the device status word (see pkv_get_device_status). */
@@ -184,6 +185,24 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* 
                            int num_blocks, pkv_dtype kv_dtype, pkv_stream_t stream);
 
 /*
+ * Swapping ("...Mathematical Foundations" §6 Preemption and Memory Recovery:
+ * evict blocks from GPU HBM to host memory and bring them back): for every
+ * pair i, block pairs[i][1] of the destination pool becomes a byte copy of
+ * block pairs[i][0] of the source pool, K and V, in one launch.  Either pool
+ * may be pinned (page-locked) host memory -- on Grace-based systems the GPU
+ * reads and writes it directly over NVLink-C2C -- or device memory; so may the
+ * pairs array.  Pageable or unmapped host memory is refused
+ * (PKV_ERR_INVALID_ARG) before any launch.  Both pools have the layout of the
+ * cache ([blocks][kv heads][B][d]) with their own block counts.  Ids outside a
+ * pool are skipped and flagged PKV_DEV_BAD_PAIR; the dst ids must be distinct.
+ */
+PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks,
+                                   void* dst_k, void* dst_v, int dst_num_blocks,
+                                   const int32_t* src_dst_pairs, int num_pairs,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   pkv_dtype kv_dtype, pkv_stream_t stream);
+
+/*
  * Paged decode attention without a caller-provided workspace.  No
  * counterpart on the pages: this entry point exists for callers that cannot
  * allocate device memory at decode time (code running while a CUDA graph is
@@ -220,6 +239,62 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
  * for the device's work to finish.  `host_code` is a host pointer.
  */
 PKV_API pkv_status pkv_get_device_status(unsigned int* host_code);
+
+/* ------------------------------------------------------------------------
+ * Host block manager ("...Mathematical Foundations" §4 Virtual Memory
+ * Architecture and Block Tables, Allocation Lifecycle; §5 Parallel Sampling
+ * and Beam Search).  Plain host code: no GPU, no CUDA calls.  It hands out
+ * physical block ids from a FIFO free list, keeps a reference count per block
+ * and a block table + token count per sequence, and tells the caller which
+ * slot each new token goes to and which copy-on-write copies to run first.
+ * Not thread-safe: one manager per scheduler thread.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager over blocks [0, num_blocks).  `free_order` (host, may be NULL)
+ * lists the ids of the initial free list in hand-out order (num_free entries,
+ * no repeats; blocks not listed are never handed out); NULL means 0, 1, ...
+ * Returns NULL on bad arguments or allocation failure. */
+PKV_API pkv_block_manager* pkv_bm_create(int num_blocks, int block_size,
+                                         const int32_t* free_order, int num_free);
+PKV_API void pkv_bm_destroy(pkv_block_manager* m);
+/* Free blocks left, or -1 for a NULL manager. */
+PKV_API int pkv_bm_num_free(const pkv_block_manager* m);
+/* Reference count of a block (0 = free), or -1 for a bad id. */
+PKV_API int pkv_bm_refcount(const pkv_block_manager* m, int32_t block);
+
+/* Prefill: a new sequence holding num_tokens tokens in ceil(num_tokens / B)
+ * fresh blocks (their slots are table[t / B] * B + t % B).  Fails with
+ * PKV_ERR_INVALID_ARG for a known id, PKV_ERR_OUT_OF_BLOCKS without changes. */
+PKV_API pkv_status pkv_bm_add_sequence(pkv_block_manager* m, int64_t seq_id,
+                                       int64_t num_tokens);
+/* Fork (parallel sampling, beam search): `child` shares every block of
+ * `parent`; each shared block's reference count goes up by one. */
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager* m, int64_t parent, int64_t child);
+/* Slot of the sequence's next token, growing the table on overflow.  If the
+ * token's block is shared (reference count > 1) it is first replaced by a
+ * fresh private block: *cow_src / *cow_dst receive the copy the caller must
+ * run (pkv_copy_blocks) before writing; otherwise both are -1. */
+PKV_API pkv_status pkv_bm_append_slot(pkv_block_manager* m, int64_t seq_id, int64_t* slot,
+                                      int32_t* cow_src, int32_t* cow_dst);
+/* Completion / pruning: drop the sequence; blocks reaching count 0 go to the
+ * back of the free list. */
+PKV_API pkv_status pkv_bm_free_sequence(pkv_block_manager* m, int64_t seq_id);
+/* The sequence's block table (up to max_blocks entries, rest -1; table may be
+ * NULL), its number of blocks and tokens. */
+PKV_API pkv_status pkv_bm_sequence(const pkv_block_manager* m, int64_t seq_id,
+                                   int32_t* table, int max_blocks, int* num_blocks,
+                                   int64_t* num_tokens);
+/* One decode step for n distinct sequences: append one token to each (in the
+ * given order), writing slot_mapping[n], the copy-on-write pairs
+ * cow_pairs[*num_cow][2] (room for n), and optionally the updated block_tables
+ * [n][max_blocks] (-1 padded) and context_lens[n].  Validates first: on error
+ * nothing changes (the free-block check assumes every append into a shared
+ * block copies, so it may refuse when exactly enough blocks remain). */
+PKV_API pkv_status pkv_bm_prepare_step(pkv_block_manager* m, const int64_t* seq_ids, int n,
+                                       int64_t* slot_mapping, int32_t* cow_pairs,
+                                       int* num_cow, int32_t* block_tables, int max_blocks,
+                                       int32_t* context_lens);
 
 /* Static description of a pkv_status. */
 PKV_API const char* pkv_status_string(pkv_status status);

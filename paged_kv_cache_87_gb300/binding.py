@@ -8,8 +8,8 @@ cannot be loaded the calls raise.
 Functions carry the C names:
   pkv_decode_workspace_bytes, pkv_paged_decode_attention,
   pkv_paged_decode_attention_noalloc, pkv_reshape_and_cache, pkv_copy_blocks,
-  pkv_get_device_status,
-  pkv_status_string, pkv_version.
+  pkv_get_device_status, pkv_status_string, pkv_version,
+and the host block manager pkv_bm_* (wrapped by ``BlockManager``).
 """
 from __future__ import annotations
 
@@ -24,7 +24,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2, 3
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+(PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA,
+ PKV_ERR_OUT_OF_BLOCKS) = range(6)
 DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT = (
     0x1, 0x2, 0x4, 0x8, 0x10)
 
@@ -50,6 +51,30 @@ _SIGNATURES = {
         ctypes.c_int,
         [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_int, ctypes.c_void_p]),
     "pkv_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
+    "pkv_swap_blocks": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p]),
+    "pkv_bm_create": (ctypes.c_void_p, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                        ctypes.c_int]),
+    "pkv_bm_destroy": (None, [ctypes.c_void_p]),
+    "pkv_bm_num_free": (ctypes.c_int, [ctypes.c_void_p]),
+    "pkv_bm_refcount": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
+    "pkv_bm_add_sequence": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]),
+    "pkv_bm_fork": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64]),
+    "pkv_bm_append_slot": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64,
+                                          ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32)]),
+    "pkv_bm_free_sequence": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64]),
+    "pkv_bm_sequence": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_int64)]),
+    "pkv_bm_prepare_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.POINTER(ctypes.c_int), ctypes.c_void_p,
+                                           ctypes.c_int, ctypes.c_void_p]),
     "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_version": (ctypes.c_int, []),
 }
@@ -252,6 +277,43 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
     _check("pkv_copy_blocks", st)
 
 
+def pkv_swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,
+                    dst_v: torch.Tensor, src_dst_pairs, stream=None) -> None:
+    """Copy blocks between two pools (device or pinned host): dst[p[1]] = src[p[0]].
+
+    Pools are [blocks, kv heads, B, d]; a host pool must be pinned
+    (``tensor.pin_memory()``).  Host pairs are validated and staged in a pinned
+    buffer; a CUDA or pinned tensor is used as is.
+    """
+    NBs, Hkv, B, d = src_k.shape
+    NBd = dst_k.shape[0]
+    if tuple(dst_k.shape[1:]) != (Hkv, B, d) or src_v.shape != src_k.shape or \
+            dst_v.shape != dst_k.shape:
+        raise ValueError("pools must be [blocks, kv heads, B, d] with matching rows")
+    for t, n in ((src_k, "src_k"), (src_v, "src_v"), (dst_k, "dst_k"), (dst_v, "dst_v")):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be a contiguous CUDA or pinned host tensor")
+    if isinstance(src_dst_pairs, torch.Tensor) and (src_dst_pairs.is_cuda or
+                                                    src_dst_pairs.is_pinned()):
+        pairs = src_dst_pairs
+    else:
+        host = np.ascontiguousarray(np.asarray(src_dst_pairs, dtype=np.int32).reshape(-1, 2))
+        if host.size and (host[:, 0].min() < 0 or host[:, 0].max() >= NBs or
+                          host[:, 1].min() < 0 or host[:, 1].max() >= NBd):
+            raise ValueError("swap_blocks: block id outside its pool")
+        if len(set(host[:, 1].tolist())) != len(host):
+            raise ValueError("swap_blocks: a destination block repeats")
+        pairs = torch.from_numpy(host).pin_memory()
+    n = pairs.numel() // 2
+    st = load().pkv_swap_blocks(src_k.data_ptr(), src_v.data_ptr(), NBs, dst_k.data_ptr(),
+                                dst_v.data_ptr(), NBd, pairs.data_ptr() if n else None, n, Hkv,
+                                d, B, dtype_code(src_k), _stream_ptr(stream))
+    _check("pkv_swap_blocks", st)
+    if not (isinstance(src_dst_pairs, torch.Tensor)) and n:
+        # the launch reads the staged pairs asynchronously: keep them alive until it ran
+        (stream or torch.cuda.current_stream()).synchronize()
+
+
 def pkv_get_device_status() -> int:
     """Read and clear the current device's status word (PKV_DEV_* bits). Synchronous."""
     v = ctypes.c_uint(0)
@@ -265,3 +327,78 @@ def pkv_status_string(status: int) -> str:
 
 def pkv_version() -> int:
     return int(load().pkv_version())
+
+
+# ----------------------------------------------------------- block manager --
+
+class BlockManager:
+    """The library's host block manager (C ABI pkv_bm_*): free list, reference
+    counts, block tables, slots and copy-on-write pairs for the device kernels."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        lib = load()
+        self.block_size = block_size
+        self.num_blocks = num_blocks
+        if free_order is None:
+            h = lib.pkv_bm_create(num_blocks, block_size, None, 0)
+        else:
+            order = np.ascontiguousarray(free_order, dtype=np.int32)
+            h = lib.pkv_bm_create(num_blocks, block_size, order.ctypes.data, int(order.size))
+        if not h:
+            raise ValueError("pkv_bm_create: bad arguments")
+        self._h = ctypes.c_void_p(h)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.pkv_bm_destroy(h)
+            self._h = None
+
+    @property
+    def num_free(self) -> int:
+        return int(load().pkv_bm_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(load().pkv_bm_refcount(self._h, int(block)))
+
+    def add_sequence(self, seq_id: int, num_tokens: int) -> None:
+        _check("pkv_bm_add_sequence", load().pkv_bm_add_sequence(self._h, seq_id, num_tokens))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pkv_bm_fork", load().pkv_bm_fork(self._h, parent, child))
+
+    def append_slot(self, seq_id: int):
+        """(slot, (src, dst) copy-on-write pair or None) of the sequence's next token."""
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check("pkv_bm_append_slot", load().pkv_bm_append_slot(
+            self._h, seq_id, ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst)))
+        return int(slot.value), (None if src.value < 0 else (int(src.value), int(dst.value)))
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pkv_bm_free_sequence", load().pkv_bm_free_sequence(self._h, seq_id))
+
+    def sequence(self, seq_id: int):
+        """(block table as a list, number of tokens)."""
+        nb, nt = ctypes.c_int(), ctypes.c_int64()
+        _check("pkv_bm_sequence", load().pkv_bm_sequence(self._h, seq_id, None, 0,
+                                                          ctypes.byref(nb), ctypes.byref(nt)))
+        table = np.zeros(max(1, nb.value), dtype=np.int32)
+        _check("pkv_bm_sequence", load().pkv_bm_sequence(
+            self._h, seq_id, table.ctypes.data, int(table.size), ctypes.byref(nb),
+            ctypes.byref(nt)))
+        return table[:nb.value].tolist(), int(nt.value)
+
+    def prepare_step(self, seq_ids, max_blocks: int):
+        """Append one token to each sequence: (slot_mapping int64[n], cow_pairs int32[k, 2],
+        block_tables int32[n, max_blocks], context_lens int32[n])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = int(ids.size)
+        slots = np.zeros(n, np.int64)
+        pairs = np.zeros((max(n, 1), 2), np.int32)
+        tables = np.zeros((max(n, 1), max_blocks), np.int32)
+        ctx = np.zeros(max(n, 1), np.int32)
+        ncow = ctypes.c_int(0)
+        _check("pkv_bm_prepare_step", load().pkv_bm_prepare_step(
+            self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
+            ctypes.byref(ncow), tables.ctypes.data, max_blocks, ctx.ctypes.data))
+        return slots, pairs[:ncow.value].copy(), tables[:n], ctx[:n]

@@ -251,9 +251,52 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_
         return PKV_ERR_INVALID_ARG;
     DeviceInfo* dev = nullptr;
     if (device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    CopyParams p{k_cache, v_cache, src_dst_pairs, dev->status,
+    CopyParams p{k_cache, v_cache, k_cache, v_cache, src_dst_pairs, dev->status,
                  (int64_t)num_kv_heads * block_size * head_dim * dtype_bytes(kv_dtype),
-                 num_blocks};
+                 num_blocks, num_blocks};
+    return cuda_status(launch_copy_blocks(p, num_pairs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int src_num_blocks,
+                           void* dst_k, void* dst_v, int dst_num_blocks,
+                           const int32_t* src_dst_pairs, int num_pairs, int num_kv_heads,
+                           int head_dim, int block_size, pkv_dtype kv_dtype,
+                           pkv_stream_t stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype_bytes(kv_dtype) == 0) return PKV_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs) return PKV_ERR_INVALID_ARG;
+    if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) ||
+        !aligned(dst_v, 16) || !aligned(src_dst_pairs, 4))
+        return PKV_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    // every buffer must be reachable from this device: device memory, or pinned
+    // host memory mapped into the device's address space
+    const void* in[5] = {src_k, src_v, dst_k, dst_v, src_dst_pairs};
+    void* mapped[5];
+    for (int i = 0; i < 5; ++i) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, in[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_INVALID_ARG;
+        }
+        if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+            mapped[i] = const_cast<void*>(in[i]);
+        } else if (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr) {
+            mapped[i] = a.devicePointer;
+        } else {
+            return PKV_ERR_INVALID_ARG;   // pageable or unmapped host memory
+        }
+    }
+    CopyParams p{mapped[0], mapped[1], mapped[2], mapped[3],
+                 static_cast<const int32_t*>(mapped[4]), dev->status,
+                 (int64_t)num_kv_heads * block_size * head_dim * dtype_bytes(kv_dtype),
+                 src_num_blocks, dst_num_blocks};
     return cuda_status(launch_copy_blocks(p, num_pairs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -279,6 +322,7 @@ const char* pkv_status_string(pkv_status status) {
     case PKV_ERR_UNSUPPORTED: return "unsupported head_dim, block_size, dtype or length";
     case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_OUT_OF_BLOCKS: return "no free KV blocks left";
     default: return "unknown status";
     }
 }

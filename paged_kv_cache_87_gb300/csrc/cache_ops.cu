@@ -1,4 +1,4 @@
-// cache_ops.cu -- the two indexing kernels that feed paged decode attention.
+// cache_ops.cu -- the kernels that write the paged KV cache.
 //
 //  * reshape_and_cache ("PagedAttention: Mathematical Foundations ..." §7
 //    kernel 1, "Fused Reshape and Block Write"): each new token's key and
@@ -6,9 +6,11 @@
 //    FP8 e4m3 with a per-tensor scale.
 //  * copy_blocks (§5 Parallel Sampling step 4 and §7 kernel 3, "Batched Block
 //    Copy-on-Write"): every copy-on-write block copy of a step in one launch.
-//
-// Both are pure data movement: one thread moves one 16-byte chunk per
-// iteration with vector loads/stores, in a grid-stride loop sized to the SMs.
+//  * swap_blocks (§6 Preemption, swapping): the same batched block copy
+//    between two pools, one of which may be pinned host memory that the GPU
+//    reaches directly (NVLink-C2C on Grace-based systems).
+// All are pure data movement: one thread moves one 16-byte chunk per
+// iteration with vector loads/stores, in a grid-stride loop.
 #include "cache_ops.cuh"
 
 namespace pkv {
@@ -98,17 +100,19 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(ReshapeParams p)
 }
 
 // grid = (pairs, slices of a block, 2 caches); one 16-byte chunk per thread-iteration.
+// Block pairs[i][0] of the source pool -> block pairs[i][1] of the destination.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
     const int pair = blockIdx.x;
     const int32_t src = p.pairs[2 * pair], dst = p.pairs[2 * pair + 1];
-    if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+    if (src < 0 || src >= p.src_num_blocks || dst < 0 || dst >= p.dst_num_blocks) {
         if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
             set_status(p.status, PKV_DEV_BAD_PAIR);
         return;
     }
-    uint8_t* cache = static_cast<uint8_t*>(blockIdx.z == 0 ? p.k_cache : p.v_cache);
-    const uint4* s = reinterpret_cast<const uint4*>(cache + (int64_t)src * p.block_bytes);
-    uint4* d = reinterpret_cast<uint4*>(cache + (int64_t)dst * p.block_bytes);
+    const uint8_t* sc = static_cast<const uint8_t*>(blockIdx.z == 0 ? p.src_k : p.src_v);
+    uint8_t* dc = static_cast<uint8_t*>(blockIdx.z == 0 ? p.dst_k : p.dst_v);
+    const uint4* s = reinterpret_cast<const uint4*>(sc + (int64_t)src * p.block_bytes);
+    uint4* d = reinterpret_cast<uint4*>(dc + (int64_t)dst * p.block_bytes);
     const int64_t n = p.block_bytes / 16;
     for (int64_t i = (int64_t)blockIdx.y * blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.y * blockDim.x)

@@ -17,12 +17,14 @@ struct ReshapeParams {
 };
 
 struct CopyParams {
-    void* k_cache;
-    void* v_cache;
+    const void* src_k;    // source pool (device memory or mapped pinned host memory)
+    const void* src_v;
+    void* dst_k;          // destination pool (same pool for copy-on-write)
+    void* dst_v;
     const int32_t* pairs;
     unsigned* status;
     int64_t block_bytes;   // num_kv_heads * block_size * head_dim * element bytes
-    int num_blocks;
+    int src_num_blocks, dst_num_blocks;
 };
 
 cudaError_t launch_reshape_and_cache(const ReshapeParams& p, pkv_dtype src, bool quant,

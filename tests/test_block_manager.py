@@ -1,0 +1,161 @@
+"""The library's host block manager (C++, pkv_bm_*), on CPU.
+
+Pinned to the pages' worked examples ("PagedAttention: Mathematical
+Foundations ..." §4 block-table diagram, §5 copy-on-write diagram), to the
+allocation lifecycle invariants of §4, and to the Python block-manager
+fixture used by the workload generator (differential test on random
+operation sequences).
+"""
+import numpy as np
+import pytest
+
+from paged_kv_cache_87_gb300 import binding, build, inputs
+from tests.helpers import ints, read_golden
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.load()
+
+
+def test_block_table_worked_example():
+    g = read_golden("block_table_example.txt")
+    B = int(g["block_size"])
+    table = ints(g["table"])
+    m = binding.BlockManager(32, B, free_order=table + [b for b in range(32) if b not in table])
+    m.add_sequence(7, int(g["num_tokens"]))
+    got, n = m.sequence(7)
+    assert got == table and n == int(g["num_tokens"])
+    # the next token (the 11th) goes to slot 19*4 + 2; a new block only after 12
+    slot, cow = m.append_slot(7)
+    assert slot == 19 * B + 2 and cow is None
+    assert m.num_free == 32 - 3
+
+
+def test_copy_on_write_worked_example():
+    g = read_golden("cow_example.txt")
+    B = int(g["block_size"])
+    m = binding.BlockManager(16, B, free_order=[7, 1, 3] + [b for b in range(16)
+                                                          if b not in (7, 1, 3)])
+    m.add_sequence(1, int(g["prompt_tokens"]))
+    m.fork(1, 2)
+    assert [m.refcount(b) for b in ints(g["prompt_table"])] == ints(g["refcount_after_fork"])
+    slot, cow = m.append_slot(1)              # sample 1 writes into shared block 1
+    assert list(cow) == ints(g["cow_pair"])
+    assert slot == 3 * B + int(g["prompt_tokens"]) % B
+    assert m.sequence(1)[0] == ints(g["sample1_table"])
+    assert m.sequence(2)[0] == ints(g["sample2_table"])
+    for b in (7, 1, 3):
+        assert m.refcount(b) == int(g[f"refcount_{b}"])
+    slot2, cow2 = m.append_slot(2)             # sample 2 now owns block 1 alone
+    assert cow2 is None and slot2 == 1 * B + int(g["prompt_tokens"]) % B
+
+
+def test_lifecycle_invariants_and_free_order():
+    B, NB = 16, 40
+    m = binding.BlockManager(NB, B)
+    m.add_sequence(0, 33)                     # 3 blocks
+    assert m.sequence(0) == ([0, 1, 2], 33)
+    for _ in range(15):                       # fills block 2 (48 tokens)
+        assert m.append_slot(0)[1] is None
+    assert m.sequence(0)[1] == 48 and len(m.sequence(0)[0]) == 3
+    m.append_slot(0)                          # overflow -> block 3
+    assert m.sequence(0)[0] == [0, 1, 2, 3]
+    m.fork(0, 1)
+    m.free_sequence(0)
+    assert m.num_free == NB - 4 and all(m.refcount(b) == 1 for b in range(4))
+    m.free_sequence(1)                        # freed blocks go to the back of the free list
+    assert m.num_free == NB
+    m.add_sequence(2, (NB - 4) * B)
+    assert m.sequence(2)[0] == list(range(4, NB))
+
+
+def test_errors_leave_state_unchanged():
+    m = binding.BlockManager(4, 8)
+    m.add_sequence(0, 24)
+    with pytest.raises(binding.PagedKVError) as e:
+        m.add_sequence(1, 17)
+    assert e.value.status == binding.PKV_ERR_OUT_OF_BLOCKS
+    m.fork(0, 1)
+    m.fork(0, 2)
+    # three appends: 0 overflows (needs a block), 1 and 2 too -> only one block left
+    with pytest.raises(binding.PagedKVError):
+        m.prepare_step([0, 1, 2], 8)
+    assert m.num_free == 1 and m.sequence(0)[1] == 24 and m.refcount(0) == 3
+    with pytest.raises(binding.PagedKVError):
+        m.fork(0, 1)                          # id in use
+    with pytest.raises(binding.PagedKVError):
+        m.append_slot(99)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_matches_python_fixture_on_random_operations(seed):
+    """Same operations on the C++ manager and the generator's fixture give the same state."""
+    rng = np.random.default_rng(seed)
+    B, NB = int(rng.choice([8, 16, 32])), 200
+    order = rng.permutation(NB)
+    cpp = binding.BlockManager(NB, B, free_order=order)
+    py = inputs.BlockManager(NB, B, rng=None, guards=False)
+    py.free = [int(b) for b in order]
+    tables, lens, next_id = {}, {}, 0
+    for _ in range(300):
+        op = rng.integers(0, 4) if tables else 0
+        try:
+            if op == 0:                                   # prefill
+                n = int(rng.integers(1, 5 * B))
+                if -(-n // B) > len(py.free):
+                    continue
+                cpp.add_sequence(next_id, n)
+                tables[next_id], lens[next_id] = py.allocate(n), n
+                next_id += 1
+            elif op == 1:                                 # fork
+                parent = int(rng.choice(list(tables)))
+                cpp.fork(parent, next_id)
+                tables[next_id], lens[next_id] = py.fork(tables[parent]), lens[parent]
+                next_id += 1
+            elif op == 2:                                 # append one token
+                sid = int(rng.choice(list(tables)))
+                t, n = tables[sid], lens[sid]
+                need = n // B >= len(t) or py.refcount[t[n // B]] > 1
+                if need and not py.free:
+                    continue
+                slot, cow = cpp.append_slot(sid)
+                pair = None
+                if n // B < len(t):
+                    pair = py.copy_on_write(t, n // B)
+                ref_slot = py.append_slot(t, n)
+                lens[sid] = n + 1
+                assert slot == ref_slot and cow == pair
+            else:                                         # completion / pruning
+                sid = int(rng.choice(list(tables)))
+                cpp.free_sequence(sid)
+                py.free_table(tables.pop(sid))
+                lens.pop(sid)
+        except binding.PagedKVError:
+            raise
+        for sid in tables:
+            assert cpp.sequence(sid) == (tables[sid], lens[sid])
+        assert cpp.num_free == len(py.free)
+        for b in range(NB):
+            assert cpp.refcount(b) == py.refcount[b]
+        # §4: waste only in the last block of each sequence
+        for sid, t in tables.items():
+            assert 0 <= len(t) * B - lens[sid] <= B - 1
+
+
+def test_prepare_step_batches_appends_and_cow():
+    B = 16
+    m = binding.BlockManager(64, B)
+    m.add_sequence(0, 40)                  # 3 blocks, last partial
+    for c in (1, 2, 3):
+        m.fork(0, c)
+    slots, pairs, tables, ctx = m.prepare_step([0, 1, 2, 3], 8)
+    # the first three writers copy the shared partial block; the last keeps it
+    assert len(pairs) == 3 and all(p[0] == 2 for p in pairs)
+    assert len(set(pairs[:, 1].tolist())) == 3 and 2 not in pairs[:, 1]
+    assert (ctx == 41).all()
+    assert tables[3, 2] == 2 and slots[3] == 2 * B + 40 % B
+    assert sorted(tables[:3, 2].tolist()) == sorted(pairs[:, 1].tolist())
+    assert (tables[:, :2] == [0, 1]).all() and (tables[:, 3:] == -1).all()
+    binding.validate_pairs(pairs, 64)
