@@ -144,6 +144,28 @@ PKV_API pkv_status pkv_paged_decode_attention(const void* query, const void* k_c
                                       pkv_stream_t stream);
 
 /*
+ * Prefix-aware decode: the same result as pkv_paged_decode_attention (same
+ * arguments, workspace size and errors), for batches in which sequences
+ * share the physical blocks of a common prompt ("...Mathematical
+ * Foundations" §5 Parallel Sampling and System Prompt Prefix Sharing).
+ * Consecutive sequences whose block-table rows start with the same physical
+ * block are grouped (at most 16 query heads per kv head in a group); the
+ * blocks every member's row shares with the first member's are streamed
+ * once for the whole group, and each member's remaining tokens separately;
+ * the two parts are merged per (sequence, query head).  Grouping applies when
+ * q and K/V are 16-bit or FP8 with 16-bit q (head_dim 128 for FP8) and a kv
+ * head has at most 8 query heads; otherwise this is the plain decode.  The
+ * rounding differs from the plain call's (the summation is split
+ * differently), within the same tolerances.
+ */
+PKV_API pkv_status pkv_paged_decode_attention_prefix(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+    pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale, void* workspace,
+    size_t workspace_bytes, void* out, pkv_stream_t stream);
+
+/*
  * Write new tokens' keys and values into their cache slots
  * ("...Mathematical Foundations" §7 kernel 1; §4 Allocation Lifecycle step 2).
  *

@@ -7,7 +7,7 @@ cannot be loaded the calls raise.
 
 Functions carry the C names:
   pkv_decode_workspace_bytes, pkv_paged_decode_attention,
-  pkv_paged_decode_attention_noalloc, pkv_reshape_and_cache, pkv_copy_blocks,
+  pkv_paged_decode_attention_prefix, pkv_paged_decode_attention_noalloc, pkv_reshape_and_cache, pkv_copy_blocks,
   pkv_get_device_status, pkv_status_string, pkv_version,
 and the host block manager pkv_bm_* (wrapped by ``BlockManager``).
 """
@@ -33,6 +33,12 @@ DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_BAD_SLOT, DEV_BAD_PAIR, DEV_WAIT_TIMEOUT 
 _SIGNATURES = {
     "pkv_decode_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int] * 6 + [ctypes.c_int]),
     "pkv_paged_decode_attention": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_float, ctypes.c_void_p,
+                                                     ctypes.c_size_t, ctypes.c_void_p,
+                                                     ctypes.c_void_p]),
+    "pkv_paged_decode_attention_prefix": (
         ctypes.c_int,
         [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_float, ctypes.c_void_p,
@@ -153,12 +159,15 @@ def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cac
                                block_tables: torch.Tensor, context_lens: torch.Tensor,
                                max_context_len: int, scale: float, kv_scale: float = 1.0,
                                workspace: torch.Tensor | None = None,
-                               out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                               out: torch.Tensor | None = None, stream=None,
+                               prefix: bool = False) -> torch.Tensor:
     """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s over context_lens[s] tokens.
 
     query [S, Hq, d]; k_cache / v_cache [NB, Hkv, B, d] (float8_e4m3fn or uint8
     for FP8); block_tables int32 [S, max_blocks]; context_lens int32 [S].
     ``workspace`` (uint8, >= pkv_decode_workspace_bytes) is allocated if None.
+    ``prefix=True`` calls pkv_paged_decode_attention_prefix (shared prompts
+    read once per group of sequences).
     """
     S, Hq, d = query.shape
     NB, Hkv, B, d2 = k_cache.shape
@@ -177,12 +186,13 @@ def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cac
         out = torch.empty_like(query)
     _cuda(out, "out")
     _cuda(workspace, "workspace")
-    st = load().pkv_paged_decode_attention(
+    fn = "pkv_paged_decode_attention_prefix" if prefix else "pkv_paged_decode_attention"
+    st = getattr(load(), fn)(
         query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), S, Hq, Hkv, d, B, NB, block_tables.shape[1],
         int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
-    _check("pkv_paged_decode_attention", st)
+    _check(fn, st)
     return out
 
 

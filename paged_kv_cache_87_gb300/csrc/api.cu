@@ -60,8 +60,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Plan {
     int group, hpi, nsub;
     int chunk_tokens, max_chunks, part_stride;
-    size_t off_hdr, off_ctx, off_items, off_prefix, off_workers, off_units, off_pm, off_pl,
-        off_pacc, total;
+    size_t off_hdr, off_ctx, off_items, off_recp, off_recc, off_workers, off_seq, off_units,
+        off_expect, off_segoff, off_pm, off_pl, off_pacc, total;
 };
 
 // Chunk length: at least 512 tokens, a multiple of 64 (every stage size and
@@ -83,20 +83,26 @@ pkv_status make_plan(int S, int Hq, int Hkv, int HD, int B, int max_ctx, Plan* p
     p.max_chunks = max_ctx > 0 ? (max_ctx + C - 1) / C : 1;
     // partial states per (sequence, query head): a fixed-chunk split has at most
     // max_chunks; a balanced split (quota >= one chunk) cuts a unit into at most
-    // max_chunks + 1 segments
-    p.part_stride = p.max_chunks + 1;
+    // max_chunks + 1 segments, and a sequence in a shared-prefix group merges
+    // the segments of its group's shared unit and of its private unit
+    p.part_stride = 2 * (p.max_chunks + 1);
     const size_t s = (size_t)S, mc = (size_t)p.max_chunks;
+    const size_t units = s * Hkv * p.nsub;      // nsub of the CUDA-core split: an upper bound
     size_t off = 0;
     p.off_hdr = off;     off += 256;
     p.off_ctx = off;     off = round_up(off + s * 4, 256);
     p.off_items = off;   off = round_up(off + s * mc * 8, 256);
-    p.off_prefix = off;  off = round_up(off + (s + 1) * 4, 256);
+    p.off_recp = off;    off = round_up(off + (2 * s + 1) * 4, 256);
+    p.off_recc = off;    off = round_up(off + 2 * s * 4, 256);
     p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 4, 256);
-    p.off_units = off;   off = round_up(off + s * Hkv * p.nsub * 4, 256);
-    const size_t partial_states = p.max_chunks > 1 ? s * Hq * (size_t)p.part_stride : 0;
-    p.off_pm = off;     off = round_up(off + partial_states * 4, 256);
-    p.off_pl = off;     off = round_up(off + partial_states * 4, 256);
-    p.off_pacc = off;   off = round_up(off + partial_states * HD * 4, 256);
+    p.off_seq = off;     off = round_up(off + 6 * s * 4, 256);   // 6 per-sequence arrays
+    p.off_units = off;   off = round_up(off + units * 4, 256);
+    p.off_expect = off;  off = round_up(off + units * 4, 256);
+    p.off_segoff = off;  off = round_up(off + units * 4, 256);
+    const size_t partial_states = max_ctx > 0 ? s * Hq * (size_t)p.part_stride : 0;
+    p.off_pm = off;      off = round_up(off + partial_states * 4, 256);
+    p.off_pl = off;      off = round_up(off + partial_states * 4, 256);
+    p.off_pacc = off;    off = round_up(off + partial_states * HD * 4, 256);
     p.total = off;
     *pl = p;
     return PKV_OK;
@@ -121,14 +127,17 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     return p.total;
 }
 
-pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, const void* v_cache,
-                                      const int32_t* block_tables, const int32_t* context_lens,
-                                      int num_seqs, int num_q_heads, int num_kv_heads,
-                                      int head_dim, int block_size, int num_blocks,
-                                      int max_blocks_per_seq, int max_context_len, float scale,
-                                      pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale,
-                                      void* workspace, size_t workspace_bytes, void* out,
-                                      pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+pkv_status decode_impl(const void* query, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+                       pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale, void* workspace,
+                       size_t workspace_bytes, void* out, pkv_stream_t stream,
+                       int allow_groups) {
     if (num_seqs < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0)
         return PKV_ERR_INVALID_ARG;
     if (q_dtype != PKV_F32 && q_dtype != PKV_F16 && q_dtype != PKV_BF16)
@@ -168,8 +177,21 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     p.ws.quota = reinterpret_cast<int*>(p.ws.counter + 2);
     p.ws.ctx_eff = reinterpret_cast<int*>(ws + plan.off_ctx);
     p.ws.items = reinterpret_cast<int2*>(ws + plan.off_items);
-    p.ws.tile_prefix = reinterpret_cast<int*>(ws + plan.off_prefix);
-    p.ws.worker_seq = reinterpret_cast<int*>(ws + plan.off_workers);
+    p.ws.rec_prefix = reinterpret_cast<int*>(ws + plan.off_recp);
+    p.ws.rec_code = reinterpret_cast<int*>(ws + plan.off_recc);
+    p.ws.worker_rec = reinterpret_cast<int*>(ws + plan.off_workers);
+    {
+        int* seq = reinterpret_cast<int*>(ws + plan.off_seq);
+        const size_t S = (size_t)num_seqs;
+        p.ws.seq_start = seq;
+        p.ws.seq_group = seq + S;
+        p.ws.grp_members = seq + 2 * S;
+        p.ws.grp_shared = seq + 3 * S;
+        p.ws.seq_rec = seq + 4 * S;
+        p.ws.grp_rec = seq + 5 * S;
+    }
+    p.ws.unit_expect = reinterpret_cast<int*>(ws + plan.off_expect);
+    p.ws.unit_segoff = reinterpret_cast<int*>(ws + plan.off_segoff);
     p.ws.unit_done = reinterpret_cast<unsigned*>(ws + plan.off_units);
     p.ws.pm = reinterpret_cast<float*>(ws + plan.off_pm);
     p.ws.pl = reinterpret_cast<float*>(ws + plan.off_pl);
@@ -188,6 +210,7 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     p.chunk_tokens = plan.chunk_tokens;
     p.max_chunks = plan.max_chunks;
     p.part_stride = plan.part_stride;
+    p.allow_groups = allow_groups;
     const bool fp8 = kv_dtype == PKV_FP8_E4M3;
     p.qk_scale_log2 = scale * 1.4426950408889634f * (fp8 ? kv_scale : 1.f);
     p.out_scale = fp8 ? kv_scale : 1.f;
@@ -208,6 +231,36 @@ pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, co
     default: err = decode_dispatch_bf16(p, kv_dtype, hpi, s); break;
     }
     return cuda_status(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attention(const void* query, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks,
+                                      int max_blocks_per_seq, int max_context_len, float scale,
+                                      pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale,
+                                      void* workspace, size_t workspace_bytes, void* out,
+                                      pkv_stream_t stream) {
+    return decode_impl(query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype, kv_scale,
+                       workspace, workspace_bytes, out, stream, 0);
+}
+
+pkv_status pkv_paged_decode_attention_prefix(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+    pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale, void* workspace,
+    size_t workspace_bytes, void* out, pkv_stream_t stream) {
+    return decode_impl(query, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype, kv_scale,
+                       workspace, workspace_bytes, out, stream, 1);
 }
 
 pkv_status pkv_reshape_and_cache(const void* key, const void* value, void* k_cache,

@@ -41,6 +41,8 @@ constexpr int kMaxItemBlocks = 64;     // table entries a producer holds per ite
 constexpr float kRescaleSlack = 8.0f;  // log2-domain headroom before moving the max
 constexpr int kMmaHeadsPerItem = 8;    // query heads per item of the tensor-core variant
 constexpr int kMaxWorkers = 4096;      // CTAs of the balanced-split decode, at most
+constexpr int kGroupRecord = 1 << 30;  // record code flag: a shared-prefix group
+constexpr int kMaxGroupHeads = 16;     // query heads a shared-prefix unit serves
 constexpr int kTileTokens = 64;        // split granularity of the balanced split
 
 struct DecodeWork {
@@ -48,10 +50,20 @@ struct DecodeWork {
     unsigned* total;      // number of work indices (dynamic items)
     int* quota;           // tiles per worker (balanced split)
     int* ctx_eff;         // [S] context length after clamping
-    int2* items;          // [S * max_chunks] (sequence, chunk)
-    int* tile_prefix;     // [S + 1] tiles of 64 tokens x units, exclusive prefix (balanced split)
-    int* worker_seq;      // [kMaxWorkers] first sequence of each worker (balanced split)
-    unsigned* unit_done;  // [S * Hkv * nsub] chunks finished
+    int2* items;          // [S * max_chunks] (sequence, chunk)            (dynamic items)
+    // balanced split with shared-prefix groups (tensor-core kernel)
+    int* rec_prefix;      // [2S + 1] tile prefix over work records
+    int* rec_code;        // [2S] record: sequence id, or group leader | kGroupRecord
+    int* worker_rec;      // [kMaxWorkers] record holding each worker's first tile
+    int* seq_start;       // [S] first private token (shared-prefix length of its group)
+    int* seq_group;       // [S] leader of its prefix group, -1 if none
+    int* grp_members;     // [S] members of the group led by this sequence (0: none)
+    int* grp_shared;      // [S] shared tokens of the group led by this sequence
+    int* seq_rec;         // [S] first tile of the sequence's private record
+    int* grp_rec;         // [S] first tile of the record of the group led by this sequence
+    int* unit_expect;     // [S * Hkv * nsub] partial states to merge per unit
+    int* unit_segoff;     // [S * Hkv * nsub] index of the unit's first private state
+    unsigned* unit_done;  // [S * Hkv * nsub] chunks / segments finished
     float* pm;            // [S * Hq * part_stride]
     float* pl;            // [S * Hq * part_stride]
     float* pacc;          // [S * Hq * part_stride * d]
@@ -71,6 +83,7 @@ struct DecodeParams {
     int chunk_tokens, max_chunks;
     int part_stride;      // partial states per (sequence, query head) in the workspace
     int num_workers;      // CTAs of the balanced-split decode
+    int allow_groups;     // group sequences that share leading blocks (prefix-aware decode)
     float qk_scale_log2;  // scale * log2(e) (* kv_scale for FP8)
     float out_scale;      // kv_scale for FP8, else 1
 };
@@ -175,7 +188,7 @@ struct StageMeta {
     int flags;                  // kFirst | kLast | kDone
     int pad[7];
 };
-constexpr int kFirst = 1, kLast = 2, kDone = 4;
+constexpr int kFirst = 1, kLast = 2, kDone = 4, kGroup = 8;
 
 template <typename Cfg>
 struct SimtSmem {

@@ -45,15 +45,18 @@ cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
 }
 
 // Tensor-core variant: 16-bit q, 16-bit or FP8 K/V, 8 query heads per item.
-template <typename QT, typename KT, int HD>
-cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
-    using Cfg = MmaCfg<QT, KT, HD>;
+// The prefix-aware entry point groups sequences that share leading blocks
+// (up to 16 query heads per shared unit) when a kv head has at most 8 query
+// heads: the NT = 2 kernel.  Otherwise NT = 1.
+template <typename QT, typename KT, int HD, int NT>
+cudaError_t launch_decode_mma_nt(const DecodeParams& p, cudaStream_t stream) {
+    using Cfg = MmaCfg<QT, KT, HD, NT>;
     static OccCache occ;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kernel = decode_mma_kernel<QT, KT, HD>;
+    auto kernel = decode_mma_kernel<QT, KT, HD, NT>;
     if (occ.ctas[dev] == 0) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)Cfg::SMEM);
@@ -78,6 +81,12 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     kernel<<<ps.num_workers, Cfg::THREADS, Cfg::SMEM, stream>>>(ps, tk, tv);
     return cudaGetLastError();
+}
+
+template <typename QT, typename KT, int HD>
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+    return p.allow_groups && p.nsub == 1 ? launch_decode_mma_nt<QT, KT, HD, 2>(p, stream)
+                                         : launch_decode_mma_nt<QT, KT, HD, 1>(p, stream);
 }
 
 template <typename QT, typename KT>

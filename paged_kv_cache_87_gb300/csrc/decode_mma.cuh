@@ -123,11 +123,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ------------------------------------------------------------------ config --
 
-template <typename QT, typename KT, int HD>
+template <typename QT, typename KT, int HD, int NT = 1>
 struct MmaCfg {
     static constexpr bool FP8 = std::is_same<KT, E4M3>::value;
     using MT = typename std::conditional<FP8, F16, KT>::type;   // mma operand type
-    static constexpr int HPI = kMmaHeadsPerItem;  // query heads per item (mma N = 8)
     static constexpr int TPS = 32;                // tokens per stage: two 16-token m-tiles
     static constexpr int ROWB = HD * KT::bytes;   // bytes of one K/V row
     static constexpr int HALVES = ROWB / 128;     // 128-byte column slices of a row
@@ -136,9 +135,11 @@ struct MmaCfg {
     static constexpr int MTILES = HD / 16;        // mma m-tiles of P.V (over d)
     static constexpr int HALF_BYTES = TPS * 128;  // one 128-byte slice of a stage
     static constexpr int KV_BYTES = HALVES * HALF_BYTES;
-    static constexpr int Q_BYTES = HPI * HD * 2;
+    // the 8-head kernel stages each segment's query rows with its first stage;
+    // the 16-head (prefix) kernel reads them from global memory instead
+    static constexpr int Q_BYTES = NT == 1 ? kMmaHeadsPerItem * HD * 2 : 0;
     static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 1023) / 1024 * 1024;
-    static constexpr int NSTAGE = FP8 ? 5 : (HD == 128 ? 3 : 5);
+    static constexpr int NSTAGE = HD == 128 ? (FP8 ? (NT == 1 ? 5 : 6) : 3) : (NT == 1 ? 5 : 6);
     static constexpr int THREADS = 64;            // consumer warp + producer warp
     static constexpr size_t OFF_METAS = (size_t)NSTAGE * STAGE_BYTES;
     static constexpr size_t OFF_BARS = OFF_METAS + NSTAGE * sizeof(StageMeta);
@@ -173,81 +174,284 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {
     return (uint32_t)(r * 128 + ((chunk ^ (r & 7)) << 4));
 }
 
-// Balanced-split planning (1 CTA x 1024 threads): clamp the context lengths,
-// count tiles = ceil(ctx / 64) x (kv heads x subgroups) per sequence, prefix-
-// sum them, pick the per-worker quota Q (at least one chunk of tokens), record
-// each worker's first sequence, reset the unit counters and zero the outputs
-// of empty sequences.
+// ---------------------------------------------------------------- planning --
+
+// Block-wide exclusive scan of two counters (1024 threads); returns this
+// thread's prefixes, and the block totals in *tot_a / *tot_b.
+__device__ __forceinline__ void scan2(int a, int b, int* ex_a, int* ex_b, int* tot_a, int* tot_b,
+                                      int* wa, int* wb) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int xa = a, xb = b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, xa, off);
+        const int yb = __shfl_up_sync(0xffffffffu, xb, off);
+        if (lane >= off) { xa += ya; xb += yb; }
+    }
+    if (lane == 31) { wa[warp] = xa; wb[warp] = xb; }
+    __syncthreads();
+    if (warp == 0) {
+        int va = wa[lane], vb = wb[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, va, off);
+            const int yb = __shfl_up_sync(0xffffffffu, vb, off);
+            if (lane >= off) { va += ya; vb += yb; }
+        }
+        wa[lane] = va;
+        wb[lane] = vb;
+    }
+    __syncthreads();
+    *ex_a = xa - a + (warp > 0 ? wa[warp - 1] : 0);
+    *ex_b = xb - b + (warp > 0 ? wb[warp - 1] : 0);
+    *tot_a = wa[31];
+    *tot_b = wb[31];
+    __syncthreads();   // wa / wb are reused by the next call
+}
+
+// Balanced-split planning (1 CTA x 1024 threads, sequences in tiles of 1024).
+//  1. Clamp context lengths.
+//  2. Shared-prefix groups ("...Mathematical Foundations" §5 Parallel Sampling
+//     and System Prompt Prefix Sharing): consecutive sequences whose tables
+//     start with the same physical block form runs; a run is cut into groups
+//     of at most kMaxGroupHeads / G members.  A group's shared prefix is the
+//     leading blocks every member's table has in common with the leader's,
+//     cut to the shortest member context and rounded down to 64 tokens; a
+//     group with at least 64 shared tokens gets one shared unit per kv head.
+//  3. Work records in sequence order -- a group's shared record before its
+//     leader's private record -- each unit cut into 64-token tiles; prefix
+//     sums over records; the per-worker quota Q; each worker's first record.
+//  4. Per (sequence, unit): the number of partial states its result merges
+//     (shared segments first, then private ones) and where the private ones
+//     start.  Unit counters reset; outputs of empty sequences zeroed.
 template <typename QT>
 __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
-    __shared__ int warp_sums[32];
-    __shared__ int carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ int s_ctx[1024], s_first[1024], s_run[1024], s_mem[1024], s_sh[1024];
+    __shared__ int wa[32], wb[32];
+    __shared__ int carry_rec, carry_tiles;
+    const int tid = threadIdx.x;
     const int upi = p.num_kv_heads * p.nsub;
-    if (tid == 0) carry = 0;
+    const bool can_group = p.allow_groups && p.nsub == 1 && p.group <= kMmaHeadsPerItem;
+    const int maxm = can_group ? kMaxGroupHeads / p.group : 1;
+    const int B = p.block_size;
+    if (tid == 0) carry_rec = carry_tiles = 0;
     for (int i = tid; i < p.num_seqs * upi; i += blockDim.x) p.ws.unit_done[i] = 0u;
-    const int cap = min(p.max_context_len, p.max_blocks * p.block_size);
+    const int cap = min(p.max_context_len, p.max_blocks * B);
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += blockDim.x) {
         const int s = base + tid;
-        int n = 0;
-        if (s < p.num_seqs) {
-            int ctx = p.context_lens[s];
+        const bool valid = s < p.num_seqs;
+        int ctx = 0;
+        if (valid) {
+            ctx = p.context_lens[s];
             if (ctx < 0 || ctx > cap) {
                 set_status(p.status, PKV_DEV_BAD_CONTEXT);
                 ctx = ctx < 0 ? 0 : cap;
             }
             p.ws.ctx_eff[s] = ctx;
-            n = (ctx + kTileTokens - 1) / kTileTokens * upi;
         }
-        int x = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        if (lane == 31) warp_sums[warp] = x;
+        const int32_t* row = p.block_tables + (int64_t)s * p.max_blocks;
+        s_ctx[tid] = ctx;
+        s_first[tid] = can_group && valid && ctx > 0 ? row[0] : -1 - tid;   // distinct if empty
         __syncthreads();
-        if (warp == 0) {
-            int v = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+        // run start: inclusive max-scan of (same first block as the previous ? -1 : tid)
+        const bool same = can_group && valid && tid > 0 && s_first[tid] >= 0 &&
+                          s_first[tid] == s_first[tid - 1];
+        int run = same ? -1 : tid;
+        {
+            const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, v, off);
-                if (lane >= off) v += y;
+                const int y = __shfl_up_sync(0xffffffffu, run, off);
+                if (lane >= off) run = max(run, y);
             }
-            warp_sums[lane] = v;
+            if (lane == 31) wa[warp] = run;
+            __syncthreads();
+            if (warp == 0) {
+                int v = wa[lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v = max(v, y);
+                }
+                wa[lane] = v;
+            }
+            __syncthreads();
+            if (warp > 0) run = max(run, wa[warp - 1]);
+            s_run[tid] = run;
+            __syncthreads();
+        }
+        // group leaders: every maxm-th position of a run
+        const int k = tid - run;
+        const bool is_lead = can_group && valid && k % maxm == 0 && ctx > 0;
+        // members: a warp per member compares its table row with its leader's, 128
+        // entries per step (coalesced loads, ballot for the first difference)
+        if (can_group) {
+            const int lane = tid & 31, warp = tid >> 5;
+            for (int i = warp; i < (int)blockDim.x; i += blockDim.x >> 5) {
+                const int ki = i - s_run[i];
+                const bool member = can_group && base + i < p.num_seqs && ki % maxm != 0 &&
+                                    s_ctx[i] > 0;
+                if (!member) continue;                       // warp-uniform
+                const int lp = i - ki % maxm;
+                const int32_t* ra = p.block_tables + (int64_t)(base + lp) * p.max_blocks;
+                const int32_t* rb = p.block_tables + (int64_t)(base + i) * p.max_blocks;
+                const int lim = min((s_ctx[lp] + B - 1) / B, (s_ctx[i] + B - 1) / B);
+                int common = lim;
+                for (int j0 = 0; j0 < lim; j0 += 128) {
+                    bool diff[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = j0 + 32 * u + lane;
+                        diff[u] = j < lim && ra[j] != rb[j];
+                    }
+                    int first = -1;
+#pragma unroll
+                    for (int u = 3; u >= 0; --u) {
+                        const unsigned m = __ballot_sync(0xffffffffu, diff[u]);
+                        if (m) first = j0 + 32 * u + __ffs(m) - 1;
+                    }
+                    if (first >= 0) {
+                        common = first;
+                        break;
+                    }
+                }
+                if (lane == 0) s_sh[i] = common;             // common leading blocks
+            }
         }
         __syncthreads();
-        const int incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
-        if (s < p.num_seqs) p.ws.tile_prefix[s] = carry + incl - n;
+        int members = 0, shared = 0;
+        if (is_lead) {
+            int m = 1;
+            while (m < maxm && tid + m < (int)blockDim.x && base + tid + m < p.num_seqs &&
+                   s_run[tid + m] == run && s_ctx[tid + m] > 0)
+                ++m;
+            if (m >= 2) {
+                int sh = (ctx + B - 1) / B, minctx = ctx;
+                for (int i = 1; i < m; ++i) {
+                    minctx = min(minctx, s_ctx[tid + i]);
+                    sh = min(sh, s_sh[tid + i]);
+                }
+                shared = min(sh * B, minctx) / kTileTokens * kTileTokens;
+                if (shared >= kTileTokens) members = m;
+                else shared = 0;
+            }
+        }
+        __syncthreads();                                      // s_sh is rewritten below
+        s_mem[tid] = members;
+        s_sh[tid] = shared;
         __syncthreads();
-        if (tid == blockDim.x - 1) carry += incl;
+        int leader = -1, start = 0;
+        if (can_group && valid) {
+            const int lp = run + (k / maxm) * maxm;
+            if (s_mem[lp] >= 2) {
+                leader = base + lp;
+                start = s_sh[lp];
+            }
+        }
+        const int priv_tiles = valid ? (ctx - start + kTileTokens - 1) / kTileTokens : 0;
+        const int nrec = valid ? 1 + (members >= 2) : 0;
+        const int ntiles = upi * priv_tiles + (members >= 2 ? p.num_kv_heads * shared / kTileTokens : 0);
+        int rb, tb, trec, ttiles;
+        scan2(nrec, ntiles, &rb, &tb, &trec, &ttiles, wa, wb);
+        // per-sequence tile bases (kept in shared memory for the last tile of
+        // sequences; a batch of <= 1024 sequences never leaves shared memory)
+        const int gtiles = members >= 2 ? shared / kTileTokens : 0;   // leader only
+        int pbase = 0;
+        if (valid) {
+            p.ws.seq_group[s] = leader;
+            p.ws.seq_start[s] = start;
+            p.ws.grp_members[s] = members;
+            p.ws.grp_shared[s] = shared;
+            int r = carry_rec + rb, t = carry_tiles + tb;
+            if (members >= 2) {
+                p.ws.rec_code[r] = s | kGroupRecord;
+                p.ws.rec_prefix[r] = t;
+                p.ws.grp_rec[s] = t;                       // tile base of the group record
+                ++r;
+                t += p.num_kv_heads * gtiles;
+            }
+            p.ws.rec_code[r] = s;
+            p.ws.rec_prefix[r] = t;
+            p.ws.seq_rec[s] = t;                           // tile base of the private record
+            pbase = t;
+        }
+        s_first[tid] = members >= 2 ? carry_tiles + tb : -1;   // reuse: group tile base
+        __syncthreads();
+        // per sequence, into registers first (members read their leader's entries)
+        const int lp = leader - base;
+        const int my_gbase = leader >= 0 ? s_first[lp] : -1;     // its group's tile base
+        const int my_gst = leader >= 0 ? s_sh[lp] / kTileTokens : 0;  // group tiles per unit
+        __syncthreads();
+        s_run[tid] = priv_tiles;
+        s_mem[tid] = my_gbase;
+        s_sh[tid] = my_gst;
+        s_ctx[tid] = pbase;
+        __syncthreads();
+        if (tid == 0) {
+            carry_rec += trec;
+            carry_tiles += ttiles;
+        }
         __syncthreads();
     }
-    const int total = carry;
-    const int min_q = p.chunk_tokens / kTileTokens;
-    const int q = max(min_q, (total + p.num_workers - 1) / p.num_workers);
+    const int nrec = carry_rec, total = carry_tiles;
+    const int q = max(p.chunk_tokens / kTileTokens, (total + p.num_workers - 1) / p.num_workers);
     if (tid == 0) {
-        p.ws.tile_prefix[p.num_seqs] = total;
-        *p.ws.quota = q;
+        p.ws.rec_prefix[nrec] = total;
+        p.ws.quota[0] = q;
+        p.ws.quota[1] = total;
     }
-    // worker b starts at tile b*q: record the sequence holding that tile
-    for (int s = tid; s < p.num_seqs; s += blockDim.x) {
-        const int lo = p.ws.tile_prefix[s], hi = lo + (p.ws.ctx_eff[s] + kTileTokens - 1) /
-                                                      kTileTokens * upi;
-        for (int b = (lo + q - 1) / q; b * q < hi && b < p.num_workers; ++b)
-            p.ws.worker_seq[b] = s;
+    // per sequence: its records' first workers, and the partial states its units
+    // merge (shared segments first, then private ones)
+    const bool in_smem = p.num_seqs <= (int)blockDim.x;
+    for (int idx = tid; idx < p.num_seqs * upi; idx += blockDim.x) {
+        const int s = idx / upi, u = idx % upi;
+        int pt, pbase, st, gbase;
+        if (in_smem) {
+            pt = s_run[s];
+            pbase = s_ctx[s];
+            gbase = s_mem[s];
+            st = s_sh[s];
+        } else {
+            const int ctx = p.ws.ctx_eff[s], start = p.ws.seq_start[s];
+            pt = (ctx - start + kTileTokens - 1) / kTileTokens;
+            pbase = p.ws.seq_rec[s];
+            const int ld = p.ws.seq_group[s];
+            gbase = ld >= 0 ? p.ws.grp_rec[ld] : -1;
+            st = ld >= 0 ? p.ws.grp_shared[ld] / kTileTokens : 0;
+        }
+        int np = 0, ns = 0;
+        if (pt > 0) {
+            const int us = pbase + u * pt, ue = us + pt;
+            np = (ue - 1) / q - us / q + 1;
+        }
+        if (gbase >= 0) {
+            const int gs = gbase + u * st, ge = gs + st;
+            ns = (ge - 1) / q - gs / q + 1;
+        }
+        p.ws.unit_expect[idx] = ns + np;
+        p.ws.unit_segoff[idx] = ns;
     }
-    const int row = p.num_q_heads * p.head_dim;
-    for (int s = warp; s < p.num_seqs; s += blockDim.x >> 5) {
-        if (p.ws.ctx_eff[s] != 0) continue;
-        for (int i = lane; i < row; i += 32) store_from_float<QT>(p.out, (int64_t)s * row + i, 0.f);
+    __syncthreads();
+    // each worker's first record
+    for (int r = tid; r < nrec; r += blockDim.x) {
+        const int lo = p.ws.rec_prefix[r], hi = p.ws.rec_prefix[r + 1];
+        for (int b = (lo + q - 1) / q; b * q < hi && b < p.num_workers; ++b) p.ws.worker_rec[b] = r;
+    }
+    // sequences without context: zero output (no private and no shared tiles)
+    const int rowlen = p.num_q_heads * p.head_dim;
+    for (int s = tid >> 5; s < p.num_seqs; s += blockDim.x >> 5) {
+        const bool empty = in_smem ? s_run[s] == 0 && s_sh[s] == 0 : p.ws.ctx_eff[s] == 0;
+        if (!empty) continue;
+        for (int i = tid & 31; i < rowlen; i += 32)
+            store_from_float<QT>(p.out, (int64_t)s * rowlen + i, 0.f);
     }
 }
 
-// The warp that finished the last segment of (sequence s, heads hq0..hq0+nh-1)
-// merges the segment states in order: M = max m_c, L = sum l_c 2^(m_c - M),
-// out = sum acc_c 2^(m_c - M) / L.  Lane i owns head i/4 and a quarter of d.
+// The warp that finished the last partial state of (sequence s, heads
+// hq0..hq0+nh-1) merges the states in order: M = max m_c, L = sum l_c
+// 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L.  Lane i owns head i/4 and a
+// quarter of d.
 template <typename QT, int HD>
 __device__ __noinline__ void merge_segments_warp(const DecodeParams& p, int s, int hq0, int nh,
                                                  int nseg, int lane) {
@@ -290,64 +494,102 @@ __device__ __noinline__ void merge_segments_warp(const DecodeParams& p, int s, i
     }
 }
 
+// ------------------------------------------------------------ work windows --
+
 // One window of a worker's range: at most 64 blocks of one unit.
 struct Window {
     int valid;
-    int s, kvh, qsub, nh;
-    int seg, nseg;              // segment index within the unit, segments of the unit
+    int group;                  // a shared-prefix unit (else a private one)
+    int s;                      // sequence whose table row is read (a group's leader)
+    int kvh, qsub, nh;          // kv head, head subgroup, query heads served
+    int members;                // sequences served (1 for a private unit)
+    int seg;                    // segment index within the unit
     int t0, t1;                 // logical tokens [t0, t1)
     int first, last;            // first / last window of the segment
 };
 
-// The sequence a producer is currently walking: its tile range [lo, hi) in
-// the flattened (unit, tile) order and its context length.
-struct SeqCursor {
-    int s, lo, hi, ctx;
+// The record a producer is currently walking.
+struct RecCursor {
+    int r, lo, hi;              // record index, its tile range [lo, hi)
+    int group, id, start, end;  // kind, sequence / leader, token range [start, end)
+    int members;
 };
 
-__device__ __forceinline__ void seq_load(const DecodeParams& p, SeqCursor& sc) {
-    sc.lo = __ldcg(&p.ws.tile_prefix[sc.s]);
-    sc.hi = __ldcg(&p.ws.tile_prefix[sc.s + 1]);
-    sc.ctx = __ldcg(&p.ws.ctx_eff[sc.s]);
+__device__ __forceinline__ void rec_load(const DecodeParams& p, RecCursor& rc) {
+    rc.lo = __ldcg(&p.ws.rec_prefix[rc.r]);
+    rc.hi = __ldcg(&p.ws.rec_prefix[rc.r + 1]);
+    const int code = __ldcg(&p.ws.rec_code[rc.r]);
+    rc.group = (code & kGroupRecord) != 0;
+    rc.id = code & (kGroupRecord - 1);
+    if (rc.group) {
+        rc.start = 0;
+        rc.end = __ldcg(&p.ws.grp_shared[rc.id]);
+        rc.members = __ldcg(&p.ws.grp_members[rc.id]);
+    } else {
+        rc.start = __ldcg(&p.ws.seq_start[rc.id]);
+        rc.end = __ldcg(&p.ws.ctx_eff[rc.id]);
+        rc.members = 1;
+    }
 }
 
 // The window starting at flattened tile `pos` of a worker whose range is
-// [a, end); `sc` advances in place to the sequence holding `pos` (global
-// loads only when the sequence changes).
+// [a, end); `rc` advances in place to the record holding `pos` (global loads
+// only when the record changes).
 __device__ __forceinline__ Window make_window(const DecodeParams& p, int worker, int a, int end,
-                                              int q, int pos, SeqCursor& sc) {
+                                              int q, int pos, RecCursor& rc) {
     Window w{};
     if (pos >= end) return w;
-    while (sc.hi <= pos) {
-        ++sc.s;
-        seq_load(p, sc);
+    while (rc.hi <= pos) {
+        ++rc.r;
+        rec_load(p, rc);
     }
-    const int tiles = (sc.ctx + kTileTokens - 1) / kTileTokens;
-    const int rel = pos - sc.lo;
+    const int tiles = (rc.end - rc.start + kTileTokens - 1) / kTileTokens;
+    const int rel = pos - rc.lo;
     const int u = rel / tiles, tile = rel % tiles;
     const int ustart = pos - tile, uend = ustart + tiles;
     const int wt = min(min(p.block_size, uend - pos), end - pos);   // <= 64 blocks
     w.valid = 1;
-    w.s = sc.s;
-    w.kvh = u / p.nsub;
-    w.qsub = u % p.nsub;
-    w.nh = min(kMmaHeadsPerItem, p.group - w.qsub * kMmaHeadsPerItem);
+    w.group = rc.group;
+    w.s = rc.id;
+    w.members = rc.members;
+    if (rc.group) {
+        w.kvh = u;
+        w.qsub = 0;
+        w.nh = rc.members * p.group;
+    } else {
+        w.kvh = u / p.nsub;
+        w.qsub = u % p.nsub;
+        w.nh = min(kMmaHeadsPerItem, p.group - w.qsub * kMmaHeadsPerItem);
+    }
     w.seg = worker - ustart / q;
-    w.nseg = (uend - 1) / q - ustart / q + 1;
-    w.t0 = tile * kTileTokens;
-    w.t1 = min((tile + wt) * kTileTokens, sc.ctx);
+    w.t0 = rc.start + tile * kTileTokens;
+    w.t1 = min(rc.start + (tile + wt) * kTileTokens, rc.end);
     w.first = pos == a || pos == ustart;
     w.last = pos + wt == end || pos + wt == uend;
     return w;
 }
 
-template <typename QT, typename KT, int HD>
+// Sequence and query head of head slot j of a window's unit.
+__device__ __forceinline__ void slot_head(const DecodeParams& p, int group, int s, int kvh,
+                                          int qsub, int j, int* seq, int* qhead) {
+    if (group) {
+        *seq = s + j / p.group;
+        *qhead = kvh * p.group + j % p.group;
+    } else {
+        *seq = s;
+        *qhead = kvh * p.group + qsub * kMmaHeadsPerItem + j;
+    }
+}
+
+// --------------------------------------------------------------------- kernel --
+
+template <typename QT, typename KT, int HD, int NT>
 __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                                         const __grid_constant__ CUtensorMap tmK,
                                                         const __grid_constant__ CUtensorMap tmV) {
-    using Cfg = MmaCfg<QT, KT, HD>;
+    using Cfg = MmaCfg<QT, KT, HD, NT>;
     using MT = typename Cfg::MT;
-    constexpr int HPI = Cfg::HPI, TPS = Cfg::TPS;
+    constexpr int TPS = Cfg::TPS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -366,8 +608,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     __syncthreads();
 
     const int B = p.block_size;
-    const int q = *p.ws.quota;
-    const int total = p.ws.tile_prefix[p.num_seqs];
+    const int q = p.ws.quota[0], total = p.ws.quota[1];   // written by the planning kernel
     const int a = blockIdx.x * q, end = min(a + q, total);
 
     if (warp == 1) {
@@ -380,9 +621,10 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        SeqCursor sc{a < end ? p.ws.worker_seq[blockIdx.x] : 0, 0, 0, 0};
-        if (a < end) seq_load(p, sc);
-        Window win = make_window(p, blockIdx.x, a, end, q, a, sc);
+        RecCursor rc{};
+        rc.r = a < end ? p.ws.worker_rec[blockIdx.x] : 0;
+        if (a < end) rec_load(p, rc);
+        Window win = make_window(p, blockIdx.x, a, end, q, a, rc);
         int pos = a;
         int e0 = 0, e1 = 0;
         if (win.valid) {
@@ -402,10 +644,10 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 if (e0 < 0 || e0 >= p.num_blocks) e0 = 0;
                 if (e1 < 0 || e1 >= p.num_blocks) e1 = 0;
             }
-            const int h0 = win.kvh * p.group + win.qsub * HPI;
             const int nstages = (win.t1 - win.t0 + TPS - 1) / TPS;
             for (int st = 0; st < nstages; ++st) {
                 const int ts = win.t0 + st * TPS, te = min(ts + TPS, win.t1);
+                const bool first = win.first && st == 0;
                 if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                     set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
                     ok = false;
@@ -413,14 +655,13 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 }
                 uint8_t* sbase = smem + (size_t)stage * Cfg::STAGE_BYTES;
                 const int fb = ts / B, nblk = (te - 1) / B - fb + 1;   // whole blocks
-                const bool qstage = win.first && st == 0;
-                const uint32_t qbytes = qstage ? (uint32_t)(win.nh * HD * 2) : 0u;
+                const uint32_t qbytes = NT == 1 && first ? (uint32_t)(win.nh * HD * 2) : 0u;
                 if (lane == 0) {
                     StageMeta& m = metas[stage];
                     m.s = win.s; m.kvh = win.kvh; m.qsub = win.qsub; m.nh = win.nh;
-                    m.chunk = win.seg; m.nchunks = win.nseg; m.ts = ts; m.te = te;
-                    m.flags = (qstage ? kFirst : 0) |
-                              (win.last && st == nstages - 1 ? kLast : 0);
+                    m.chunk = win.seg; m.nchunks = win.members; m.ts = ts; m.te = te;
+                    m.flags = (first ? kFirst : 0) | (win.last && st == nstages - 1 ? kLast : 0) |
+                              (win.group ? kGroup : 0);
                     mbar_arrive_expect_tx(&full[stage],
                                           2u * (uint32_t)(nblk * B) * Cfg::ROWB + qbytes);
                 }
@@ -441,7 +682,8 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                     &tmV, x, y, &full[stage], policy);
                     }
                 }
-                if (qstage && lane == 31) {
+                if (qbytes && lane == 31) {
+                    const int h0 = win.kvh * p.group + win.qsub * kMmaHeadsPerItem;
                     const int64_t qoff = ((int64_t)win.s * p.num_q_heads + h0) * HD * 2;
                     bulk_g2s(sbase + 2 * Cfg::KV_BYTES, (const uint8_t*)p.q + qoff, qbytes,
                              &full[stage]);
@@ -450,7 +692,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 if (st == 0) {
                     // look one window ahead once this window's first stage is in flight:
                     // its block-table entries load while this window streams
-                    nxt = make_window(p, blockIdx.x, a, end, q, pos + wtiles, sc);
+                    nxt = make_window(p, blockIdx.x, a, end, q, pos + wtiles, rc);
                     if (nxt.valid) {
                         const int32_t* trow = p.block_tables + (int64_t)nxt.s * p.max_blocks;
                         const int nj0 = nxt.t0 / B, nnb = (nxt.t1 + B - 1) / B - nj0;
@@ -479,11 +721,12 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
 
     // ========================= consumer warp =========================
     const int g = lane >> 2, c = lane & 3;
-    uint32_t qf[Cfg::KSTEPS][2];      // Q^T B fragments
-    float o[Cfg::MTILES][4];          // O^T C fragments, rows mapped to d by d_row()
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qf[NT][Cfg::KSTEPS][2];   // Q^T B fragments, n-tile nt = head slots 8nt..8nt+7
+    float o[Cfg::MTILES][NT][4];       // O^T C fragments, rows mapped to d by d_row()
+    float m0[NT], m1[NT], l0[NT], l1[NT];
     int stage = 0;
     uint32_t phase = 0;
+    int nt_live = 1;
     // d index of C-fragment row g (half 0) or g + 8 (half 1) of P.V m-tile mt
     auto d_row = [&](int mt, int half) -> int {
         if constexpr (Cfg::FP8) return 32 * (mt >> 1) + 2 * g + (mt & 1) + 16 * half;
@@ -502,25 +745,37 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         const uint32_t sV = sK + Cfg::KV_BYTES;
 
         if (meta.flags & kFirst) {
-            const uint32_t* sQ = reinterpret_cast<const uint32_t*>(sbase + 2 * Cfg::KV_BYTES);
-            const bool live = g < meta.nh;
+            // Q^T fragments: from the stage (8-head kernel, rows staged by the producer)
+            // or straight from global memory (16-head kernel; small and L2-resident)
+            const uint32_t* qg = static_cast<const uint32_t*>(p.q);
+            if constexpr (NT == 1) qg = reinterpret_cast<const uint32_t*>(sbase + 2 * Cfg::KV_BYTES);
+            nt_live = meta.nh > 8 ? 2 : 1;
+            const bool grp = (meta.flags & kGroup) != 0;
 #pragma unroll
-            for (int t = 0; t < Cfg::KSTEPS; ++t) {
-                if constexpr (Cfg::FP8) {
-                    // k-slots (2c, 2c+1) <-> dims 16t+4c, +1; (8+2c, 9+2c) <-> 16t+4c+2, +3
-                    qf[t][0] = live ? q_pair<QT, MT>(sQ[(g * HD + 16 * t + 4 * c) >> 1]) : 0u;
-                    qf[t][1] = live ? q_pair<QT, MT>(sQ[(g * HD + 16 * t + 4 * c + 2) >> 1]) : 0u;
-                } else {
-                    qf[t][0] = live ? sQ[(g * HD + 16 * t + 2 * c) >> 1] : 0u;
-                    qf[t][1] = live ? sQ[(g * HD + 16 * t + 8 + 2 * c) >> 1] : 0u;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hs = nt * 8 + g;                 // head slot of this lane's n column
+                const bool live = hs < meta.nh;
+                int seq = 0, qh = 0;
+                slot_head(p, grp, meta.s, meta.kvh, meta.qsub, live ? hs : 0, &seq, &qh);
+                const int64_t rowq = NT == 1 ? (int64_t)hs * HD                     // staged rows
+                                             : ((int64_t)seq * p.num_q_heads + qh) * HD;
+#pragma unroll
+                for (int t = 0; t < Cfg::KSTEPS; ++t) {
+                    if constexpr (Cfg::FP8) {
+                        qf[nt][t][0] = live ? q_pair<QT, MT>(qg[(rowq + 16 * t + 4 * c) >> 1]) : 0u;
+                        qf[nt][t][1] = live ? q_pair<QT, MT>(qg[(rowq + 16 * t + 4 * c + 2) >> 1]) : 0u;
+                    } else {
+                        qf[nt][t][0] = live ? qg[(rowq + 16 * t + 2 * c) >> 1] : 0u;
+                        qf[nt][t][1] = live ? qg[(rowq + 16 * t + 8 + 2 * c) >> 1] : 0u;
+                    }
                 }
+#pragma unroll
+                for (int mt = 0; mt < Cfg::MTILES; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+                m0[nt] = m1[nt] = -INFINITY;
+                l0[nt] = l1[nt] = 0.f;
             }
-#pragma unroll
-            for (int mt = 0; mt < Cfg::MTILES; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
         }
 
         const int nvalid = meta.te - meta.ts;            // 1..32
@@ -537,13 +792,17 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
             __syncwarp();
         }
         const bool two = nvalid > 16;                    // second m-tile holds tokens
-        // ---- S^T = K . Q^T for the stage's (up to) two 16-token m-tiles ----
-        float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // ---- S^T = K . Q^T: (up to) two 16-token m-tiles x (up to) NT 8-head n-tiles ----
+        float sa[2][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[mt][nt][e] = 0.f;
         {
             const int rl = (lane & 7) + ((lane >> 3) & 1) * 8;
             if constexpr (Cfg::FP8) {
-                // one 16-byte chunk = 16 e4m3 dims = one k-step; a lane's 4 bytes of a
-                // row feed its k-slots (2c, 2c+1) and (8+2c, 9+2c)
 #pragma unroll
                 for (int pr = 0; pr < Cfg::KSTEPS / 2; ++pr) {
                     const int chunk = 2 * pr + (lane >> 4);
@@ -559,7 +818,11 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                                    e4m3x2_to_f16x2(hi & 0xffffu),
                                                    e4m3x2_to_f16x2(lo >> 16),
                                                    e4m3x2_to_f16x2(hi >> 16)};
-                            Mma<MT>::run(sa[mt], a, qf[2 * pr + k][0], qf[2 * pr + k][1]);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                if (nt < nt_live)
+                                    Mma<MT>::run(sa[mt][nt], a, qf[nt][2 * pr + k][0],
+                                                 qf[nt][2 * pr + k][1]);
                         }
                     }
                 }
@@ -568,71 +831,73 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 for (int t = 0; t < Cfg::KSTEPS; ++t) {
                     const int half = t >> 2, chunk = (t & 3) * 2 + (lane >> 4);
                     const uint32_t base = sK + half * Cfg::HALF_BYTES;
-                    uint32_t a[4];
-                    ldsm_x4(base + swz(rl, chunk), a);
-                    Mma<MT>::run(sa[0], a, qf[t][0], qf[t][1]);
-                    if (two) {
-                        uint32_t b[4];
-                        ldsm_x4(base + swz(16 + rl, chunk), b);
-                        Mma<MT>::run(sa[1], b, qf[t][0], qf[t][1]);
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        if (mt == 1 && !two) break;
+                        uint32_t a[4];
+                        ldsm_x4(base + swz(16 * mt + rl, chunk), a);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            if (nt < nt_live) Mma<MT>::run(sa[mt][nt], a, qf[nt][t][0], qf[nt][t][1]);
                     }
                 }
             }
         }
-        // ---- online softmax over the stage's tokens ----
-        float x[2][4];
+        // ---- online softmax over the stage's tokens, per n-tile ----
+        uint32_t pb[2][NT][2];   // P^T B fragments: k-step (tokens 0-15 / 16-31) x n-tile
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            const bool va = mt * 16 + g < nvalid, vb = mt * 16 + g + 8 < nvalid;
-            x[mt][0] = va ? sa[mt][0] * p.qk_scale_log2 : -INFINITY;
-            x[mt][1] = va ? sa[mt][1] * p.qk_scale_log2 : -INFINITY;
-            x[mt][2] = vb ? sa[mt][2] * p.qk_scale_log2 : -INFINITY;
-            x[mt][3] = vb ? sa[mt][3] * p.qk_scale_log2 : -INFINITY;
-        }
-        float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
-        float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+        for (int nt = 0; nt < NT; ++nt) {
+            if (nt >= nt_live) break;
+            float x[2][4];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const bool n0 = mx0 > m0 + kRescaleSlack, n1 = mx1 > m1 + kRescaleSlack;
-        if (__any_sync(0xffffffffu, n0 || n1)) {
-            const float r0 = n0 ? fast_exp2(m0 - mx0) : 1.f;
-            const float r1 = n1 ? fast_exp2(m1 - mx1) : 1.f;
-            if (n0) m0 = mx0;
-            if (n1) m1 = mx1;
-            l0 *= r0;
-            l1 *= r1;
-#pragma unroll
-            for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-                o[mt][0] *= r0;
-                o[mt][2] *= r0;
-                o[mt][1] *= r1;
-                o[mt][3] *= r1;
+            for (int mt = 0; mt < 2; ++mt) {
+                const bool va = mt * 16 + g < nvalid, vb = mt * 16 + g + 8 < nvalid;
+                x[mt][0] = va ? sa[mt][nt][0] * p.qk_scale_log2 : -INFINITY;
+                x[mt][1] = va ? sa[mt][nt][1] * p.qk_scale_log2 : -INFINITY;
+                x[mt][2] = vb ? sa[mt][nt][2] * p.qk_scale_log2 : -INFINITY;
+                x[mt][3] = vb ? sa[mt][nt][3] * p.qk_scale_log2 : -INFINITY;
             }
-        }
-        uint32_t pb[2][2];   // P^T B fragments of the two k-steps (tokens 0-15, 16-31)
+            float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+            float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            float f0, f1, f2, f3;
-            const uint32_t p01 =
-                Mma<MT>::pack(fast_exp2(x[mt][0] - m0), fast_exp2(x[mt][1] - m1), f0, f1);
-            const uint32_t p23 =
-                Mma<MT>::pack(fast_exp2(x[mt][2] - m0), fast_exp2(x[mt][3] - m1), f2, f3);
-            l0 += f0 + f2;
-            l1 += f1 + f3;
-            pb[mt][0] = movmatrix_trans(p01);
-            pb[mt][1] = movmatrix_trans(p23);
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const bool n0 = mx0 > m0[nt] + kRescaleSlack, n1 = mx1 > m1[nt] + kRescaleSlack;
+            if (__any_sync(0xffffffffu, n0 || n1)) {
+                const float r0 = n0 ? fast_exp2(m0[nt] - mx0) : 1.f;
+                const float r1 = n1 ? fast_exp2(m1[nt] - mx1) : 1.f;
+                if (n0) m0[nt] = mx0;
+                if (n1) m1[nt] = mx1;
+                l0[nt] *= r0;
+                l1[nt] *= r1;
+#pragma unroll
+                for (int mt = 0; mt < Cfg::MTILES; ++mt) {
+                    o[mt][nt][0] *= r0;
+                    o[mt][nt][2] *= r0;
+                    o[mt][nt][1] *= r1;
+                    o[mt][nt][3] *= r1;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                float f0, f1, f2, f3;
+                const uint32_t p01 = Mma<MT>::pack(fast_exp2(x[mt][0] - m0[nt]),
+                                                   fast_exp2(x[mt][1] - m1[nt]), f0, f1);
+                const uint32_t p23 = Mma<MT>::pack(fast_exp2(x[mt][2] - m0[nt]),
+                                                   fast_exp2(x[mt][3] - m1[nt]), f2, f3);
+                l0[nt] += f0 + f2;
+                l1[nt] += f1 + f3;
+                pb[mt][nt][0] = movmatrix_trans(p01);
+                pb[mt][nt][1] = movmatrix_trans(p23);
+            }
         }
         // ---- O^T += V^T . P^T ----
         {
             const int mi = lane >> 3;
             const int rv = (lane & 7) + (mi >> 1) * 8;
             if constexpr (Cfg::FP8) {
-                // a transposed 8x8 b16 block of e4m3 rows gives each lane V[2c][2g, 2g+1]
-                // and V[2c+1][2g, 2g+1]; byte permutes split them into an even-d and an
-                // odd-d A fragment (m-tiles 2pr and 2pr+1 over dims 32pr .. 32pr+31)
 #pragma unroll
                 for (int pr = 0; pr < Cfg::MTILES / 2; ++pr) {
                     const int chunk = 2 * pr + (mi & 1);
@@ -647,8 +912,12 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                             ev[k] = e4m3x2_to_f16x2(__byte_perm(r[k], 0u, 0x0020));
                             od[k] = e4m3x2_to_f16x2(__byte_perm(r[k], 0u, 0x0031));
                         }
-                        Mma<MT>::run(o[2 * pr], ev, pb[ks][0], pb[ks][1]);
-                        Mma<MT>::run(o[2 * pr + 1], od, pb[ks][0], pb[ks][1]);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            if (nt >= nt_live) break;
+                            Mma<MT>::run(o[2 * pr][nt], ev, pb[ks][nt][0], pb[ks][nt][1]);
+                            Mma<MT>::run(o[2 * pr + 1][nt], od, pb[ks][nt][0], pb[ks][nt][1]);
+                        }
                     }
                 }
             } else {
@@ -656,13 +925,15 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 for (int mt = 0; mt < Cfg::MTILES; ++mt) {
                     const int half = mt >> 2, chunk = (mt & 3) * 2 + (mi & 1);
                     const uint32_t base = sV + half * Cfg::HALF_BYTES;
-                    uint32_t a[4];
-                    ldsm_x4_trans(base + swz(rv, chunk), a);
-                    Mma<MT>::run(o[mt], a, pb[0][0], pb[0][1]);
-                    if (two) {
-                        uint32_t b[4];
-                        ldsm_x4_trans(base + swz(16 + rv, chunk), b);
-                        Mma<MT>::run(o[mt], b, pb[1][0], pb[1][1]);
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        if (ks == 1 && !two) break;
+                        uint32_t a[4];
+                        ldsm_x4_trans(base + swz(16 * ks + rv, chunk), a);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            if (nt < nt_live)
+                                Mma<MT>::run(o[mt][nt], a, pb[ks][nt][0], pb[ks][nt][1]);
                     }
                 }
             }
@@ -674,62 +945,78 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         if (!(meta.flags & kLast)) continue;
 
         // ---------------- end of the segment (warp-local) ----------------
+        const bool grp = (meta.flags & kGroup) != 0;
+        const int upi = p.num_kv_heads * p.nsub;
+        unsigned last_mask = 0;   // lane i of lane 0's loop: unit i finished
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
-        const int hq0 = meta.kvh * p.group + meta.qsub * HPI;
-        const int ha = 2 * c, hb = 2 * c + 1;
-        const int64_t sha = (int64_t)meta.s * p.num_q_heads + hq0 + ha;
-        const int64_t shb = sha + 1;
-        if (meta.nchunks == 1) {
-            const float ia = l0 > 0.f ? p.out_scale / l0 : 0.f;
-            const float ib = l1 > 0.f ? p.out_scale / l1 : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            if (nt >= nt_live) break;
 #pragma unroll
-            for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-                const int d0 = d_row(mt, 0), d1 = d_row(mt, 1);
-                if (ha < meta.nh) {
-                    store_from_float<QT>(p.out, sha * HD + d0, o[mt][0] * ia);
-                    store_from_float<QT>(p.out, sha * HD + d1, o[mt][2] * ia);
+            for (int off = 4; off < 32; off <<= 1) {
+                l0[nt] += __shfl_xor_sync(0xffffffffu, l0[nt], off);
+                l1[nt] += __shfl_xor_sync(0xffffffffu, l1[nt], off);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int j = nt * 8 + 2 * c + hh;        // head slot of this lane's column
+                if (j >= meta.nh) continue;
+                int seq, qh;
+                slot_head(p, grp, meta.s, meta.kvh, meta.qsub, j, &seq, &qh);
+                const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
+                const int expect = __ldcg(&p.ws.unit_expect[unit]);
+                const int64_t sh = (int64_t)seq * p.num_q_heads + qh;
+                const float lsum = hh ? l1[nt] : l0[nt];
+                const float msum = hh ? m1[nt] : m0[nt];
+                if (expect == 1) {
+                    // this segment is the head's whole context: write the output
+                    const float inv = lsum > 0.f ? p.out_scale / lsum : 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < Cfg::MTILES; ++mt) {
+                        store_from_float<QT>(p.out, sh * HD + d_row(mt, 0), o[mt][nt][hh] * inv);
+                        store_from_float<QT>(p.out, sh * HD + d_row(mt, 1),
+                                             o[mt][nt][2 + hh] * inv);
+                    }
+                } else {
+                    const int idx = (grp ? 0 : __ldcg(&p.ws.unit_segoff[unit])) + meta.chunk;
+                    const int64_t pi = sh * p.part_stride + idx;
+#pragma unroll
+                    for (int mt = 0; mt < Cfg::MTILES; ++mt) {
+                        p.ws.pacc[pi * HD + d_row(mt, 0)] = o[mt][nt][hh];
+                        p.ws.pacc[pi * HD + d_row(mt, 1)] = o[mt][nt][2 + hh];
+                    }
+                    if (g == 0) {
+                        p.ws.pm[pi] = msum;
+                        p.ws.pl[pi] = lsum;
+                    }
                 }
-                if (hb < meta.nh) {
-                    store_from_float<QT>(p.out, shb * HD + d0, o[mt][1] * ib);
-                    store_from_float<QT>(p.out, shb * HD + d1, o[mt][3] * ib);
-                }
             }
-            continue;
-        }
-        const int64_t pa_i = sha * p.part_stride + meta.chunk;
-        const int64_t pb_i = shb * p.part_stride + meta.chunk;
-#pragma unroll
-        for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-            const int d0 = d_row(mt, 0), d1 = d_row(mt, 1);
-            if (ha < meta.nh) {
-                p.ws.pacc[pa_i * HD + d0] = o[mt][0];
-                p.ws.pacc[pa_i * HD + d1] = o[mt][2];
-            }
-            if (hb < meta.nh) {
-                p.ws.pacc[pb_i * HD + d0] = o[mt][1];
-                p.ws.pacc[pb_i * HD + d1] = o[mt][3];
-            }
-        }
-        if (g == 0) {
-            if (ha < meta.nh) { p.ws.pm[pa_i] = m0; p.ws.pl[pa_i] = l0; }
-            if (hb < meta.nh) { p.ws.pm[pb_i] = m1; p.ws.pl[pb_i] = l1; }
         }
         __syncwarp();
-        int last = 0;
         if (lane == 0) {
             // the warp barrier above orders the lanes' stores before this lane's
-            // gpu-scope fence, which publishes them before the arrival
+            // gpu-scope fence, which publishes them before the arrivals
             __threadfence();
-            const int unit = (meta.s * p.num_kv_heads + meta.kvh) * p.nsub + meta.qsub;
-            last = atomicAdd(&p.ws.unit_done[unit], 1u) == (unsigned)(meta.nchunks - 1);
-            if (last) __threadfence();
+            const int nunits = grp ? meta.nchunks : 1;   // members served
+            for (int i = 0; i < nunits; ++i) {
+                const int seq = meta.s + (grp ? i : 0);
+                const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
+                const int expect = __ldcg(&p.ws.unit_expect[unit]);
+                if (expect <= 1) continue;
+                if (atomicAdd(&p.ws.unit_done[unit], 1u) == (unsigned)(expect - 1))
+                    last_mask |= 1u << i;
+            }
+            if (last_mask) __threadfence();
         }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) merge_segments_warp<QT, HD>(p, meta.s, hq0, meta.nh, meta.nchunks, lane);
+        last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
+        while (last_mask) {
+            const int i = __ffs(last_mask) - 1;
+            last_mask &= last_mask - 1;
+            const int seq = meta.s + (grp ? i : 0);
+            const int hq0 = meta.kvh * p.group + (grp ? 0 : meta.qsub * kMmaHeadsPerItem);
+            const int nh = grp ? p.group : meta.nh;
+            const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
+            merge_segments_warp<QT, HD>(p, seq, hq0, nh, __ldcg(&p.ws.unit_expect[unit]), lane);
+        }
     }
 }
 

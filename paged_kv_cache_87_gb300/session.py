@@ -46,8 +46,11 @@ def to_numpy_storage(t: torch.Tensor, dtype: str) -> np.ndarray:
 class DeviceState:
     """A workload's pool and step inputs resident on one CUDA device."""
 
-    def __init__(self, w: Workload, device="cuda", keep_vectors: bool = False):
+    def __init__(self, w: Workload, device="cuda", keep_vectors: bool = False,
+                 prefix: bool | None = None):
         self.w = w
+        # prefix-aware decode for workloads built with shared prompts
+        self.prefix = w.group_of_seq is not None if prefix is None else prefix
         self.device = torch.device(device)
         dev = self.device
         self.k_cache = poisoned_cache(w.cache_shape, w.kv_dtype, dev)
@@ -98,7 +101,7 @@ class DeviceState:
         return binding.pkv_paged_decode_attention(
             self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
             w.max_context_len, w.scale, kv_scale=w.kv_scale, workspace=self.workspace,
-            out=self.out if out is None else out, stream=stream)
+            out=self.out if out is None else out, stream=stream, prefix=self.prefix)
 
     def step(self, stream=None) -> torch.Tensor:
         """One pass of the hot path: copy-on-write, append the new tokens, decode."""

@@ -104,12 +104,14 @@ def tolerance(w: inputs.Workload) -> float:
     return TOL["e4m3"] if w.kv_dtype == "e4m3" else TOL[w.q_dtype]
 
 
-def gpu_state(w: inputs.Workload, steps: int = 1):
-    """DeviceState after the workload's setup and `steps` hot-path steps."""
+def gpu_state(w: inputs.Workload, steps: int = 1, prefix: bool | None = None):
+    """DeviceState after the workload's setup and `steps` hot-path steps.
+
+    prefix: use the prefix-aware decode (default: for shared-prompt workloads)."""
     import torch
     from paged_kv_cache_87_gb300 import binding
     from paged_kv_cache_87_gb300.session import DeviceState
-    st = DeviceState(w, "cuda")
+    st = DeviceState(w, "cuda", prefix=prefix)
     st.run_setup()
     for _ in range(steps):
         st.step()

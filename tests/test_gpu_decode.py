@@ -156,17 +156,22 @@ def test_nan_poison_outside_context_is_never_read():
     assert torch.isfinite(st.out.float()).all()
 
 
-def test_shared_prefix_cow_step_is_bit_identical():
+def test_shared_prefix_cow_step_moves_no_data():
+    """The step's copy-on-write repoint changes block ids, not data: the outputs agree.
+
+    (Not bit for bit: the decode groups sequences by the physical blocks their
+    tables share, so the repoint changes how much of the prompt is read once
+    for the whole group, and with it the summation order.)"""
     w = inputs.make_config(4, num_seqs=16, ctx_cap=2000)
     st = gpu_state(w)
-    with_cow = st.out.clone()
+    with_cow = st.out_f64()
     tables = w.block_tables.copy()
     for src, dst in w.step_pairs:
         tables[tables == dst] = src
     st.block_tables.copy_(torch.from_numpy(tables))
     st.decode()
     torch.cuda.synchronize()
-    assert torch.equal(with_cow.view(torch.int16), st.out.view(torch.int16))
+    assert np.abs(st.out_f64() - with_cow).max() <= tolerance(w)
 
 
 def test_matches_dense_attention_on_logical_kv():

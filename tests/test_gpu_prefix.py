@@ -1,0 +1,114 @@
+"""Prefix-aware decode: sequences whose tables share leading blocks are grouped and the
+shared blocks are streamed once for every member ("PagedAttention: Mathematical
+Foundations ..." §5 Parallel Sampling, System Prompt Prefix Sharing).  Results must
+match the oracle, which knows nothing about sharing."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_87_gb300 import binding, inputs
+from tests.helpers import gpu_state, oracle_caches, oracle_decode, tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, prefix=True):
+    st = gpu_state(w, prefix=prefix)
+    kc, vc = oracle_caches(w)
+    ref = oracle_decode(w, kc, vc, nthreads=8)
+    err = np.abs(st.out_f64() - ref).max()
+    assert np.isfinite(st.out_f64()).all() and err <= tolerance(w), err
+    return st
+
+
+@pytest.mark.parametrize("samples,Hq,Hkv", [(2, 8, 8), (4, 32, 8), (5, 32, 8), (3, 16, 2),
+                                            (2, 16, 2), (17, 4, 4), (3, 6, 2)])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_shared_prefix_groups_bf16(samples, Hq, Hkv, B):
+    rng = np.random.default_rng(samples * 100 + Hq + B)
+    w = inputs.make_shared_prefix("prefix", rng, num_groups=3, samples=samples, prefix_lo=40,
+                                  prefix_hi=700, tail_lo=1, tail_hi=150, num_q_heads=Hq,
+                                  num_kv_heads=Hkv, head_dim=128, block_size=B, q_dtype="bf16",
+                                  kv_dtype="bf16", kv_scale=1.0, scale=1 / math.sqrt(128))
+    _check(w)
+
+
+@pytest.mark.parametrize("dt,kv,d", [("f16", "f16", 64), ("bf16", "e4m3", 128),
+                                     ("f16", "e4m3", 128)])
+def test_shared_prefix_groups_types(dt, kv, d):
+    rng = np.random.default_rng(7)
+    w = inputs.make_shared_prefix("prefix", rng, num_groups=4, samples=4, prefix_lo=64,
+                                  prefix_hi=2000, tail_lo=1, tail_hi=300, num_q_heads=32,
+                                  num_kv_heads=8, head_dim=d, block_size=16, q_dtype=dt,
+                                  kv_dtype=kv, kv_scale=2.0 ** -5 if kv == "e4m3" else 1.0,
+                                  scale=1 / math.sqrt(d))
+    _check(w)
+
+
+def test_whole_context_shared_and_mixed_batch():
+    """Members with identical tables and lengths (nothing private) next to ungrouped ones."""
+    rng = np.random.default_rng(11)
+    base = inputs.make_independent("x", rng, np.array([256, 77, 512, 300, 1000]),
+                                   num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
+                                   q_dtype="bf16", kv_dtype="bf16", scale=1 / math.sqrt(128))
+    # sequences 0,1,2 become copies of sequence 0's table and length (256 = 4 whole tiles):
+    # one group whose members have no private tokens
+    t = base.block_tables.copy()
+    ctx = base.context_lens.copy()
+    order = [0, 0, 0, 1, 2, 3, 4]
+    w = inputs.Workload(
+        name="shared", num_seqs=len(order), num_q_heads=16, num_kv_heads=4, head_dim=128,
+        block_size=16, num_blocks=base.num_blocks, q_dtype="bf16", src_dtype="bf16",
+        kv_dtype="bf16", kv_scale=1.0, scale=base.scale,
+        query=inputs.draw_normal(rng, (len(order), 16, 128), "bf16"), key=base.key,
+        value=base.value, setup=base.setup, step_pairs=base.step_pairs,
+        new_vec=base.new_vec[order], new_slots=base.new_slots[order],
+        block_tables=np.ascontiguousarray(t[order]), context_lens=np.ascontiguousarray(ctx[order]),
+        seq_tokens=[base.seq_tokens[i] for i in order])
+    st = _check(w)
+    _check(w, prefix=False)
+    # the three identical sequences differ only in their queries
+    assert not torch.equal(st.out[0], st.out[1])
+
+
+def test_plain_decode_on_shared_prompts():
+    """The plain entry point on the same shared-prompt batch (no grouping)."""
+    rng = np.random.default_rng(8)
+    w = inputs.make_shared_prefix("prefix", rng, num_groups=3, samples=4, prefix_lo=64,
+                                  prefix_hi=900, tail_lo=1, tail_hi=100, num_q_heads=16,
+                                  num_kv_heads=4, head_dim=128, block_size=16, q_dtype="bf16",
+                                  kv_dtype="bf16", kv_scale=1.0, scale=1 / math.sqrt(128))
+    _check(w, prefix=False)
+
+
+def test_grouping_is_invariant_under_block_relabeling():
+    from tests.helpers import relabel_blocks
+    w = inputs.make_config(4, num_seqs=16, ctx_cap=1500)
+    a = gpu_state(w, prefix=True).out.clone()
+    perm = np.random.default_rng(3).permutation(w.num_blocks)
+    b = gpu_state(relabel_blocks(w, perm), prefix=True).out.clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("prefix", [True, False])
+def test_batches_above_one_planner_tile(prefix):
+    """More than 1024 sequences: the planner walks several tiles of sequences."""
+    rng = np.random.default_rng(21)
+    w = inputs.make_shared_prefix("many", rng, num_groups=300, samples=4, prefix_lo=64,
+                                  prefix_hi=160, tail_lo=1, tail_hi=40, num_q_heads=8,
+                                  num_kv_heads=2, head_dim=128, block_size=16, q_dtype="bf16",
+                                  kv_dtype="bf16", kv_scale=1.0, scale=1 / math.sqrt(128))
+    assert w.num_seqs == 1200
+    _check(w, prefix=prefix)
+
+
+def test_plain_batch_above_one_planner_tile():
+    rng = np.random.default_rng(22)
+    ctx = rng.integers(0, 300, size=1300)
+    w = inputs.make_independent("many", rng, ctx, num_q_heads=16, num_kv_heads=4, head_dim=64,
+                                block_size=8, q_dtype="f16", kv_dtype="f16",
+                                scale=1 / math.sqrt(64))
+    st = _check(w, prefix=False)
+    assert (st.out_f64()[ctx == 0] == 0).all()
