@@ -61,7 +61,7 @@ struct Plan {
     int group, hpi, nsub;
     int chunk_tokens, max_chunks, part_stride;
     size_t off_hdr, off_ctx, off_items, off_recp, off_recc, off_workers, off_seq, off_units,
-        off_expect, off_segoff, off_pm, off_pl, off_pacc, total;
+        off_expect, off_pm, off_pl, off_pacc, total;
 };
 
 // Chunk length: at least 512 tokens, a multiple of 64 (every stage size and
@@ -93,12 +93,11 @@ pkv_status make_plan(int S, int Hq, int Hkv, int HD, int B, int max_ctx, Plan* p
     p.off_ctx = off;     off = round_up(off + s * 4, 256);
     p.off_items = off;   off = round_up(off + s * mc * 8, 256);
     p.off_recp = off;    off = round_up(off + (2 * s + 1) * 4, 256);
-    p.off_recc = off;    off = round_up(off + 2 * s * 4, 256);
+    p.off_recc = off;    off = round_up(off + 2 * s * 16, 256);
     p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 4, 256);
-    p.off_seq = off;     off = round_up(off + 6 * s * 4, 256);   // 6 per-sequence arrays
+    p.off_seq = off;     off = round_up(off + s * 16, 256);
     p.off_units = off;   off = round_up(off + units * 4, 256);
     p.off_expect = off;  off = round_up(off + units * 4, 256);
-    p.off_segoff = off;  off = round_up(off + units * 4, 256);
     const size_t partial_states = max_ctx > 0 ? s * Hq * (size_t)p.part_stride : 0;
     p.off_pm = off;      off = round_up(off + partial_states * 4, 256);
     p.off_pl = off;      off = round_up(off + partial_states * 4, 256);
@@ -178,20 +177,10 @@ pkv_status decode_impl(const void* query, const void* k_cache, const void* v_cac
     p.ws.ctx_eff = reinterpret_cast<int*>(ws + plan.off_ctx);
     p.ws.items = reinterpret_cast<int2*>(ws + plan.off_items);
     p.ws.rec_prefix = reinterpret_cast<int*>(ws + plan.off_recp);
-    p.ws.rec_code = reinterpret_cast<int*>(ws + plan.off_recc);
+    p.ws.rec = reinterpret_cast<int4*>(ws + plan.off_recc);
     p.ws.worker_rec = reinterpret_cast<int*>(ws + plan.off_workers);
-    {
-        int* seq = reinterpret_cast<int*>(ws + plan.off_seq);
-        const size_t S = (size_t)num_seqs;
-        p.ws.seq_start = seq;
-        p.ws.seq_group = seq + S;
-        p.ws.grp_members = seq + 2 * S;
-        p.ws.grp_shared = seq + 3 * S;
-        p.ws.seq_rec = seq + 4 * S;
-        p.ws.grp_rec = seq + 5 * S;
-    }
+    p.ws.seq_info = reinterpret_cast<int4*>(ws + plan.off_seq);
     p.ws.unit_expect = reinterpret_cast<int*>(ws + plan.off_expect);
-    p.ws.unit_segoff = reinterpret_cast<int*>(ws + plan.off_segoff);
     p.ws.unit_done = reinterpret_cast<unsigned*>(ws + plan.off_units);
     p.ws.pm = reinterpret_cast<float*>(ws + plan.off_pm);
     p.ws.pl = reinterpret_cast<float*>(ws + plan.off_pl);

@@ -33,6 +33,16 @@ __device__ __forceinline__ void set_status(unsigned int* status, unsigned int bi
     if (status) atomicOr(status, bit);
 }
 
+// Arrival on a gpu-scope counter: a release of every write that happens before
+// it (a warp barrier first makes the other lanes' writes count) and, for the
+// last arriver, an acquire of the writes the earlier arrivals released.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* ctr, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old) : "l"(ctr), "r"(v) : "memory");
+    return old;
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -53,16 +53,13 @@ struct DecodeWork {
     int2* items;          // [S * max_chunks] (sequence, chunk)            (dynamic items)
     // balanced split with shared-prefix groups (tensor-core kernel)
     int* rec_prefix;      // [2S + 1] tile prefix over work records
-    int* rec_code;        // [2S] record: sequence id, or group leader | kGroupRecord
+    int4* rec;            // [2S] record {sequence | kGroupRecord for a group's shared
+                          //   record, first token, end token, members (group) or
+                          //   first tile of its group's shared record (-1: none)}
     int* worker_rec;      // [kMaxWorkers] record holding each worker's first tile
-    int* seq_start;       // [S] first private token (shared-prefix length of its group)
-    int* seq_group;       // [S] leader of its prefix group, -1 if none
-    int* grp_members;     // [S] members of the group led by this sequence (0: none)
-    int* grp_shared;      // [S] shared tokens of the group led by this sequence
-    int* seq_rec;         // [S] first tile of the sequence's private record
-    int* grp_rec;         // [S] first tile of the record of the group led by this sequence
-    int* unit_expect;     // [S * Hkv * nsub] partial states to merge per unit
-    int* unit_segoff;     // [S * Hkv * nsub] index of the unit's first private state
+    int4* seq_info;       // [S] {private tiles per unit, first private tile, first tile
+                          //   of its group's shared record (-1: none), group tiles per unit}
+    int* unit_expect;     // [S * Hkv * nsub] partial states a grouped unit merges
     unsigned* unit_done;  // [S * Hkv * nsub] chunks / segments finished
     float* pm;            // [S * Hq * part_stride]
     float* pl;            // [S * Hq * part_stride]
@@ -186,7 +183,8 @@ struct StageMeta {
     int chunk, nchunks;         // chunk index, chunks of this sequence
     int ts, te;                 // logical tokens [ts, te) held by this stage
     int flags;                  // kFirst | kLast | kDone
-    int pad[7];
+    int expect, segoff;         // private unit: partial states merged, first private one
+    int pad[5];
 };
 constexpr int kFirst = 1, kLast = 2, kDone = 4, kGroup = 8;
 

@@ -288,26 +288,26 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         // entries per step (coalesced loads, ballot for the first difference)
         if (can_group) {
             const int lane = tid & 31, warp = tid >> 5;
-            for (int i = warp; i < (int)blockDim.x; i += blockDim.x >> 5) {
+            const int nvalid = min((int)blockDim.x, p.num_seqs - base);
+            for (int i = warp; i < nvalid; i += blockDim.x >> 5) {
                 const int ki = i - s_run[i];
-                const bool member = can_group && base + i < p.num_seqs && ki % maxm != 0 &&
-                                    s_ctx[i] > 0;
+                const bool member = ki % maxm != 0 && s_ctx[i] > 0;
                 if (!member) continue;                       // warp-uniform
                 const int lp = i - ki % maxm;
                 const int32_t* ra = p.block_tables + (int64_t)(base + lp) * p.max_blocks;
                 const int32_t* rb = p.block_tables + (int64_t)(base + i) * p.max_blocks;
                 const int lim = min((s_ctx[lp] + B - 1) / B, (s_ctx[i] + B - 1) / B);
                 int common = lim;
-                for (int j0 = 0; j0 < lim; j0 += 128) {
-                    bool diff[4];
+                for (int j0 = 0; j0 < lim; j0 += 512) {
+                    bool diff[16];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 16; ++u) {
                         const int j = j0 + 32 * u + lane;
-                        diff[u] = j < lim && ra[j] != rb[j];
+                        diff[u] = j < lim && __ldg(ra + j) != __ldg(rb + j);
                     }
                     int first = -1;
 #pragma unroll
-                    for (int u = 3; u >= 0; --u) {
+                    for (int u = 15; u >= 0; --u) {
                         const unsigned m = __ballot_sync(0xffffffffu, diff[u]);
                         if (m) first = j0 + 32 * u + __ffs(m) - 1;
                     }
@@ -354,39 +354,31 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         const int ntiles = upi * priv_tiles + (members >= 2 ? p.num_kv_heads * shared / kTileTokens : 0);
         int rb, tb, trec, ttiles;
         scan2(nrec, ntiles, &rb, &tb, &trec, &ttiles, wa, wb);
-        // per-sequence tile bases (kept in shared memory for the last tile of
-        // sequences; a batch of <= 1024 sequences never leaves shared memory)
+        const int r0 = carry_rec + rb, t0 = carry_tiles + tb;
         const int gtiles = members >= 2 ? shared / kTileTokens : 0;   // leader only
-        int pbase = 0;
-        if (valid) {
-            p.ws.seq_group[s] = leader;
-            p.ws.seq_start[s] = start;
-            p.ws.grp_members[s] = members;
-            p.ws.grp_shared[s] = shared;
-            int r = carry_rec + rb, t = carry_tiles + tb;
-            if (members >= 2) {
-                p.ws.rec_code[r] = s | kGroupRecord;
-                p.ws.rec_prefix[r] = t;
-                p.ws.grp_rec[s] = t;                       // tile base of the group record
-                ++r;
-                t += p.num_kv_heads * gtiles;
-            }
-            p.ws.rec_code[r] = s;
-            p.ws.rec_prefix[r] = t;
-            p.ws.seq_rec[s] = t;                           // tile base of the private record
-            pbase = t;
+        const int pbase = t0 + p.num_kv_heads * gtiles;                  // first private tile
+        if (valid && members >= 2) {
+            p.ws.rec[r0] = make_int4(s | kGroupRecord, 0, shared, members);
+            p.ws.rec_prefix[r0] = t0;
         }
-        s_first[tid] = members >= 2 ? carry_tiles + tb : -1;   // reuse: group tile base
+        s_first[tid] = members >= 2 ? t0 : -1;                 // reuse: group tile base
         __syncthreads();
-        // per sequence, into registers first (members read their leader's entries)
+        // members read their leader's entries: into registers before the rewrite
         const int lp = leader - base;
-        const int my_gbase = leader >= 0 ? s_first[lp] : -1;     // its group's tile base
-        const int my_gst = leader >= 0 ? s_sh[lp] / kTileTokens : 0;  // group tiles per unit
+        const int my_gbase = leader >= 0 ? s_first[lp] : -1;
+        const int my_gst = leader >= 0 ? s_sh[lp] / kTileTokens : 0;
+        if (valid) {
+            const int r = r0 + (members >= 2);
+            p.ws.rec[r] = make_int4(s, start, ctx, my_gbase);
+            p.ws.rec_prefix[r] = pbase;
+            p.ws.seq_info[s] = make_int4(priv_tiles, pbase, my_gbase, my_gst);
+        }
         __syncthreads();
+        // a batch of <= 1024 sequences keeps its per-sequence entries in shared memory
         s_run[tid] = priv_tiles;
+        s_ctx[tid] = pbase;
         s_mem[tid] = my_gbase;
         s_sh[tid] = my_gst;
-        s_ctx[tid] = pbase;
         __syncthreads();
         if (tid == 0) {
             carry_rec += trec;
@@ -401,42 +393,38 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         p.ws.quota[0] = q;
         p.ws.quota[1] = total;
     }
-    // per sequence: its records' first workers, and the partial states its units
-    // merge (shared segments first, then private ones)
+    // partial states each unit of a grouped sequence merges: its group's shared
+    // segments, then its private ones (private units carry the count in their
+    // work record's window instead)
     const bool in_smem = p.num_seqs <= (int)blockDim.x;
-    for (int idx = tid; idx < p.num_seqs * upi; idx += blockDim.x) {
-        const int s = idx / upi, u = idx % upi;
-        int pt, pbase, st, gbase;
-        if (in_smem) {
-            pt = s_run[s];
-            pbase = s_ctx[s];
-            gbase = s_mem[s];
-            st = s_sh[s];
-        } else {
-            const int ctx = p.ws.ctx_eff[s], start = p.ws.seq_start[s];
-            pt = (ctx - start + kTileTokens - 1) / kTileTokens;
-            pbase = p.ws.seq_rec[s];
-            const int ld = p.ws.seq_group[s];
-            gbase = ld >= 0 ? p.ws.grp_rec[ld] : -1;
-            st = ld >= 0 ? p.ws.grp_shared[ld] / kTileTokens : 0;
+    if (can_group) {
+        for (int idx = tid; idx < p.num_seqs * upi; idx += blockDim.x) {
+            const int s = idx / upi, u = idx % upi;
+            const int4 si = in_smem ? make_int4(s_run[s], s_ctx[s], s_mem[s], s_sh[s])
+                                    : p.ws.seq_info[s];
+            if (si.z < 0) continue;                        // not in a group
+            int np = 0;
+            if (si.x > 0) {
+                const int us = si.y + u * si.x;
+                np = (us + si.x - 1) / q - us / q + 1;
+            }
+            const int gs = si.z + u * si.w;
+            p.ws.unit_expect[idx] = (gs + si.w - 1) / q - gs / q + 1 + np;
         }
-        int np = 0, ns = 0;
-        if (pt > 0) {
-            const int us = pbase + u * pt, ue = us + pt;
-            np = (ue - 1) / q - us / q + 1;
-        }
-        if (gbase >= 0) {
-            const int gs = gbase + u * st, ge = gs + st;
-            ns = (ge - 1) / q - gs / q + 1;
-        }
-        p.ws.unit_expect[idx] = ns + np;
-        p.ws.unit_segoff[idx] = ns;
     }
     __syncthreads();
-    // each worker's first record
-    for (int r = tid; r < nrec; r += blockDim.x) {
-        const int lo = p.ws.rec_prefix[r], hi = p.ws.rec_prefix[r + 1];
-        for (int b = (lo + q - 1) / q; b * q < hi && b < p.num_workers; ++b) p.ws.worker_rec[b] = r;
+    // each worker's first record: the last record starting at or before its first
+    // tile (binary search over the record prefix)
+    for (int b = tid; b < p.num_workers; b += blockDim.x) {
+        const int pos = b * q;
+        if (pos >= total) break;
+        int lo = 0, hi = nrec - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.ws.rec_prefix[mid] <= pos) lo = mid;
+            else hi = mid - 1;
+        }
+        p.ws.worker_rec[b] = lo;
     }
     // sequences without context: zero output (no private and no shared tiles)
     const int rowlen = p.num_q_heads * p.head_dim;
@@ -448,45 +436,69 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
     }
 }
 
-// The warp that finished the last partial state of (sequence s, heads
-// hq0..hq0+nh-1) merges the states in order: M = max m_c, L = sum l_c
-// 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L.  Lane i owns head i/4 and a
-// quarter of d.
+// Merge of the partial states of up to 8 (sequence, query head) rows, one
+// row per 4 lanes (lane 4h + q holds quarter q of d of row h): M = max m_c,
+// L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L over the row's
+// nseg states, in state order.  Lanes with row < 0 idle.  Loads of several
+// states are issued together: the states sit in L2, written by other CTAs.
 template <typename QT, int HD>
-__device__ __noinline__ void merge_segments_warp(const DecodeParams& p, int s, int hq0, int nh,
-                                                 int nseg, int lane) {
+__device__ __noinline__ void merge_rows_warp(const DecodeParams& p, int64_t row, int nseg,
+                                             int lane) {
     constexpr int DQ = HD / 4;     // dims per lane: 32 or 16
-    const int h = lane >> 2, q4 = lane & 3;
-    if (h >= nh) return;
-    const int64_t sh = (int64_t)s * p.num_q_heads + hq0 + h;
-    const float* pm = p.ws.pm + sh * p.part_stride;
-    const float* pl = p.ws.pl + sh * p.part_stride;
-    const float4* pa = reinterpret_cast<const float4*>(p.ws.pacc + sh * p.part_stride * HD + q4 * DQ);
+    constexpr int NV = DQ / 4;     // float4 per lane and state
+    if (row < 0) return;
+    const int q4 = lane & 3;
+    const float* pm = p.ws.pm + row * p.part_stride;
+    const float* pl = p.ws.pl + row * p.part_stride;
+    const float4* pa = reinterpret_cast<const float4*>(p.ws.pacc + row * p.part_stride * HD) +
+                       q4 * NV;
     float M = -INFINITY;
-    for (int c = 0; c < nseg; ++c) M = fmaxf(M, __ldcg(pm + c));
+    int c = 0;
+    for (; c + 4 <= nseg; c += 4) {
+        const float a0 = __ldcg(pm + c), a1 = __ldcg(pm + c + 1);
+        const float a2 = __ldcg(pm + c + 2), a3 = __ldcg(pm + c + 3);
+        M = fmaxf(M, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
+    }
+    for (; c < nseg; ++c) M = fmaxf(M, __ldcg(pm + c));
     float L = 0.f;
-    float4 A[DQ / 4];
+    float4 A[NV];
 #pragma unroll
-    for (int k = 0; k < DQ / 4; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < nseg; ++c) {
-        const float mc = __ldcg(pm + c);
+    for (int k = 0; k < NV; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](const float4 (&v)[NV], float mc, float lc) {
         const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
-        L = fmaf(__ldcg(pl + c), f, L);
-        float4 v[DQ / 4];
+        L = fmaf(lc, f, L);
 #pragma unroll
-        for (int k = 0; k < DQ / 4; ++k) v[k] = __ldcg(pa + (int64_t)c * (HD / 4) + k);
-#pragma unroll
-        for (int k = 0; k < DQ / 4; ++k) {
+        for (int k = 0; k < NV; ++k) {
             A[k].x = fmaf(v[k].x, f, A[k].x);
             A[k].y = fmaf(v[k].y, f, A[k].y);
             A[k].z = fmaf(v[k].z, f, A[k].z);
             A[k].w = fmaf(v[k].w, f, A[k].w);
         }
+    };
+    c = 0;
+    for (; c + 2 <= nseg; c += 2) {
+        float4 v0[NV], v1[NV];
+        const float m0 = __ldcg(pm + c), m1 = __ldcg(pm + c + 1);
+        const float l0 = __ldcg(pl + c), l1 = __ldcg(pl + c + 1);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            v0[k] = __ldcg(pa + (int64_t)c * (HD / 4) + k);
+            v1[k] = __ldcg(pa + (int64_t)(c + 1) * (HD / 4) + k);
+        }
+        add(v0, m0, l0);
+        add(v1, m1, l1);
+    }
+    if (c < nseg) {
+        float4 v0[NV];
+        const float m0 = __ldcg(pm + c), l0 = __ldcg(pl + c);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) v0[k] = __ldcg(pa + (int64_t)c * (HD / 4) + k);
+        add(v0, m0, l0);
     }
     const float inv = L > 0.f ? p.out_scale / L : 0.f;
-    const int64_t o0 = sh * HD + q4 * DQ;
+    const int64_t o0 = row * HD + q4 * DQ;
 #pragma unroll
-    for (int k = 0; k < DQ / 4; ++k) {
+    for (int k = 0; k < NV; ++k) {
         store_from_float<QT>(p.out, o0 + 4 * k + 0, A[k].x * inv);
         store_from_float<QT>(p.out, o0 + 4 * k + 1, A[k].y * inv);
         store_from_float<QT>(p.out, o0 + 4 * k + 2, A[k].z * inv);
@@ -504,6 +516,7 @@ struct Window {
     int kvh, qsub, nh;          // kv head, head subgroup, query heads served
     int members;                // sequences served (1 for a private unit)
     int seg;                    // segment index within the unit
+    int expect, segoff;         // private unit: partial states merged, first private one
     int t0, t1;                 // logical tokens [t0, t1)
     int first, last;            // first / last window of the segment
 };
@@ -512,24 +525,20 @@ struct Window {
 struct RecCursor {
     int r, lo, hi;              // record index, its tile range [lo, hi)
     int group, id, start, end;  // kind, sequence / leader, token range [start, end)
-    int members;
+    int members;                // sequences served
+    int gbase;                  // private record: first tile of its group's record, or -1
 };
 
 __device__ __forceinline__ void rec_load(const DecodeParams& p, RecCursor& rc) {
     rc.lo = __ldcg(&p.ws.rec_prefix[rc.r]);
     rc.hi = __ldcg(&p.ws.rec_prefix[rc.r + 1]);
-    const int code = __ldcg(&p.ws.rec_code[rc.r]);
-    rc.group = (code & kGroupRecord) != 0;
-    rc.id = code & (kGroupRecord - 1);
-    if (rc.group) {
-        rc.start = 0;
-        rc.end = __ldcg(&p.ws.grp_shared[rc.id]);
-        rc.members = __ldcg(&p.ws.grp_members[rc.id]);
-    } else {
-        rc.start = __ldcg(&p.ws.seq_start[rc.id]);
-        rc.end = __ldcg(&p.ws.ctx_eff[rc.id]);
-        rc.members = 1;
-    }
+    const int4 e = __ldcg(&p.ws.rec[rc.r]);
+    rc.group = (e.x & kGroupRecord) != 0;
+    rc.id = e.x & (kGroupRecord - 1);
+    rc.start = e.y;
+    rc.end = e.z;
+    rc.members = rc.group ? e.w : 1;
+    rc.gbase = rc.group ? -1 : e.w;
 }
 
 // The window starting at flattened tile `pos` of a worker whose range is
@@ -556,10 +565,21 @@ __device__ __forceinline__ Window make_window(const DecodeParams& p, int worker,
         w.kvh = u;
         w.qsub = 0;
         w.nh = rc.members * p.group;
+        w.expect = -1;                           // per member: read at the segment's end
+        w.segoff = 0;                            // shared segments come first
     } else {
         w.kvh = u / p.nsub;
         w.qsub = u % p.nsub;
         w.nh = min(kMmaHeadsPerItem, p.group - w.qsub * kMmaHeadsPerItem);
+        // segments of this unit's group record (one unit per kv head), then its own
+        int ns = 0;
+        if (rc.gbase >= 0) {
+            const int gst = rc.start / kTileTokens;
+            const int gs = rc.gbase + u * gst;
+            ns = (gs + gst - 1) / q - gs / q + 1;
+        }
+        w.segoff = ns;
+        w.expect = ns + (uend - 1) / q - ustart / q + 1;
     }
     w.seg = worker - ustart / q;
     w.t0 = rc.start + tile * kTileTokens;
@@ -660,6 +680,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                     StageMeta& m = metas[stage];
                     m.s = win.s; m.kvh = win.kvh; m.qsub = win.qsub; m.nh = win.nh;
                     m.chunk = win.seg; m.nchunks = win.members; m.ts = ts; m.te = te;
+                    m.expect = win.expect; m.segoff = win.segoff;
                     m.flags = (first ? kFirst : 0) | (win.last && st == nstages - 1 ? kLast : 0) |
                               (win.group ? kGroup : 0);
                     mbar_arrive_expect_tx(&full[stage],
@@ -820,7 +841,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                                    e4m3x2_to_f16x2(hi >> 16)};
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
-                                if (nt < nt_live)
+                                if (NT == 1 || nt < nt_live)
                                     Mma<MT>::run(sa[mt][nt], a, qf[nt][2 * pr + k][0],
                                                  qf[nt][2 * pr + k][1]);
                         }
@@ -838,7 +859,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                         ldsm_x4(base + swz(16 * mt + rl, chunk), a);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            if (nt < nt_live) Mma<MT>::run(sa[mt][nt], a, qf[nt][t][0], qf[nt][t][1]);
+                            if (NT == 1 || nt < nt_live) Mma<MT>::run(sa[mt][nt], a, qf[nt][t][0], qf[nt][t][1]);
                     }
                 }
             }
@@ -847,7 +868,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         uint32_t pb[2][NT][2];   // P^T B fragments: k-step (tokens 0-15 / 16-31) x n-tile
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            if (nt >= nt_live) break;
+            if (NT > 1 && nt >= nt_live) break;
             float x[2][4];
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
@@ -914,7 +935,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                         }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            if (nt >= nt_live) break;
+                            if (NT > 1 && nt >= nt_live) break;
                             Mma<MT>::run(o[2 * pr][nt], ev, pb[ks][nt][0], pb[ks][nt][1]);
                             Mma<MT>::run(o[2 * pr + 1][nt], od, pb[ks][nt][0], pb[ks][nt][1]);
                         }
@@ -932,7 +953,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                         ldsm_x4_trans(base + swz(16 * ks + rv, chunk), a);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            if (nt < nt_live)
+                            if (NT == 1 || nt < nt_live)
                                 Mma<MT>::run(o[mt][nt], a, pb[ks][nt][0], pb[ks][nt][1]);
                     }
                 }
@@ -947,10 +968,9 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         // ---------------- end of the segment (warp-local) ----------------
         const bool grp = (meta.flags & kGroup) != 0;
         const int upi = p.num_kv_heads * p.nsub;
-        unsigned last_mask = 0;   // lane i of lane 0's loop: unit i finished
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            if (nt >= nt_live) break;
+            if (NT > 1 && nt >= nt_live) break;
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l0[nt] += __shfl_xor_sync(0xffffffffu, l0[nt], off);
@@ -962,8 +982,8 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 if (j >= meta.nh) continue;
                 int seq, qh;
                 slot_head(p, grp, meta.s, meta.kvh, meta.qsub, j, &seq, &qh);
-                const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
-                const int expect = __ldcg(&p.ws.unit_expect[unit]);
+                const int expect =
+                    grp ? __ldcg(&p.ws.unit_expect[seq * upi + meta.kvh]) : meta.expect;
                 const int64_t sh = (int64_t)seq * p.num_q_heads + qh;
                 const float lsum = hh ? l1[nt] : l0[nt];
                 const float msum = hh ? m1[nt] : m0[nt];
@@ -977,7 +997,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                              o[mt][nt][2 + hh] * inv);
                     }
                 } else {
-                    const int idx = (grp ? 0 : __ldcg(&p.ws.unit_segoff[unit])) + meta.chunk;
+                    const int idx = meta.segoff + meta.chunk;
                     const int64_t pi = sh * p.part_stride + idx;
 #pragma unroll
                     for (int mt = 0; mt < Cfg::MTILES; ++mt) {
@@ -991,31 +1011,41 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 }
             }
         }
+        // split units: lane i (< units served) arrives on unit i's counter once the
+        // warp barrier has ordered every lane's partial-state stores before it;
+        // units the segment covers whole need neither
         __syncwarp();
-        if (lane == 0) {
-            // the warp barrier above orders the lanes' stores before this lane's
-            // gpu-scope fence, which publishes them before the arrivals
-            __threadfence();
-            const int nunits = grp ? meta.nchunks : 1;   // members served
-            for (int i = 0; i < nunits; ++i) {
-                const int seq = meta.s + (grp ? i : 0);
-                const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
-                const int expect = __ldcg(&p.ws.unit_expect[unit]);
-                if (expect <= 1) continue;
-                if (atomicAdd(&p.ws.unit_done[unit], 1u) == (unsigned)(expect - 1))
-                    last_mask |= 1u << i;
-            }
-            if (last_mask) __threadfence();
+        const int nunits = grp ? meta.nchunks : 1;   // members served
+        int my_expect = 1;
+        bool last = false;
+        if (lane < nunits) {
+            const int unit = (meta.s + (grp ? lane : 0)) * upi + meta.kvh * p.nsub + meta.qsub;
+            my_expect = grp ? __ldcg(&p.ws.unit_expect[unit]) : meta.expect;
+            if (my_expect > 1)
+                last = atom_add_acq_rel_gpu(&p.ws.unit_done[unit], 1u) ==
+                       (unsigned)(my_expect - 1);
         }
-        last_mask = __shfl_sync(0xffffffffu, last_mask, 0);
+        unsigned last_mask = __ballot_sync(0xffffffffu, last);
+        if (last_mask) __syncwarp();   // the acquiring lanes' view reaches the warp
+        // merges of the units this warp finished last, whole units, <= 8 heads a pass
+        const int nh_unit = grp ? p.group : meta.nh;
         while (last_mask) {
-            const int i = __ffs(last_mask) - 1;
-            last_mask &= last_mask - 1;
-            const int seq = meta.s + (grp ? i : 0);
-            const int hq0 = meta.kvh * p.group + (grp ? 0 : meta.qsub * kMmaHeadsPerItem);
-            const int nh = grp ? p.group : meta.nh;
-            const int unit = seq * upi + meta.kvh * p.nsub + meta.qsub;
-            merge_segments_warp<QT, HD>(p, seq, hq0, nh, __ldcg(&p.ws.unit_expect[unit]), lane);
+            int64_t row = -1;
+            int nseg = 0, used = 0;
+            while (last_mask && used + nh_unit <= 8) {
+                const int i = __ffs(last_mask) - 1;
+                last_mask &= last_mask - 1;
+                const int n_i = __shfl_sync(0xffffffffu, my_expect, i);
+                const int hs = (lane >> 2) - used;
+                if (hs >= 0 && hs < nh_unit) {
+                    const int seq = meta.s + (grp ? i : 0);
+                    const int hq0 = meta.kvh * p.group + (grp ? 0 : meta.qsub * kMmaHeadsPerItem);
+                    row = (int64_t)seq * p.num_q_heads + hq0 + hs;
+                    nseg = n_i;
+                }
+                used += nh_unit;
+            }
+            merge_rows_warp<QT, HD>(p, row, nseg, lane);
         }
     }
 }
