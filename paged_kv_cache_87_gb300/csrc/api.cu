@@ -94,7 +94,7 @@ pkv_status make_plan(int S, int Hq, int Hkv, int HD, int B, int max_ctx, Plan* p
     p.off_items = off;   off = round_up(off + s * mc * 8, 256);
     p.off_recp = off;    off = round_up(off + (2 * s + 1) * 4, 256);
     p.off_recc = off;    off = round_up(off + 2 * s * 16, 256);
-    p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 4, 256);
+    p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 32, 256);
     p.off_seq = off;     off = round_up(off + s * 16, 256);
     p.off_units = off;   off = round_up(off + units * 4, 256);
     p.off_expect = off;  off = round_up(off + units * 4, 256);
@@ -178,7 +178,7 @@ pkv_status decode_impl(const void* query, const void* k_cache, const void* v_cac
     p.ws.items = reinterpret_cast<int2*>(ws + plan.off_items);
     p.ws.rec_prefix = reinterpret_cast<int*>(ws + plan.off_recp);
     p.ws.rec = reinterpret_cast<int4*>(ws + plan.off_recc);
-    p.ws.worker_rec = reinterpret_cast<int*>(ws + plan.off_workers);
+    p.ws.worker_first = reinterpret_cast<int4*>(ws + plan.off_workers);
     p.ws.seq_info = reinterpret_cast<int4*>(ws + plan.off_seq);
     p.ws.unit_expect = reinterpret_cast<int*>(ws + plan.off_expect);
     p.ws.unit_done = reinterpret_cast<unsigned*>(ws + plan.off_units);

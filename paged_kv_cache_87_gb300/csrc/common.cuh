@@ -43,6 +43,11 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* ctr, unsigned
     return old;
 }
 
+// Bring the 128-byte line holding `ptr` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

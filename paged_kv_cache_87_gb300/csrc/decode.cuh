@@ -56,7 +56,8 @@ struct DecodeWork {
     int4* rec;            // [2S] record {sequence | kGroupRecord for a group's shared
                           //   record, first token, end token, members (group) or
                           //   first tile of its group's shared record (-1: none)}
-    int* worker_rec;      // [kMaxWorkers] record holding each worker's first tile
+    int4* worker_first;   // [2 * kMaxWorkers] per worker: {record holding its first tile,
+                          //   that record's tile range [lo, hi)}, then the record itself
     int4* seq_info;       // [S] {private tiles per unit, first private tile, first tile
                           //   of its group's shared record (-1: none), group tiles per unit}
     int* unit_expect;     // [S * Hkv * nsub] partial states a grouped unit merges

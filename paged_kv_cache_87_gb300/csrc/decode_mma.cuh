@@ -253,6 +253,12 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         const int32_t* row = p.block_tables + (int64_t)s * p.max_blocks;
         s_ctx[tid] = ctx;
         s_first[tid] = can_group && valid && ctx > 0 ? row[0] : -1 - tid;   // distinct if empty
+        if (can_group && valid && ctx > 0) {
+            // the member compares below read these rows: start them towards L2 now
+            const int nb = (ctx + B - 1) / B;
+            for (int j = 32; j < nb; j += 32) prefetch_l2(row + j);
+            prefetch_l2(row + nb - 1);
+        }
         __syncthreads();
         // run start: inclusive max-scan of (same first block as the previous ? -1 : tid)
         const bool same = can_group && valid && tid > 0 && s_first[tid] >= 0 &&
@@ -424,7 +430,8 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
             if (p.ws.rec_prefix[mid] <= pos) lo = mid;
             else hi = mid - 1;
         }
-        p.ws.worker_rec[b] = lo;
+        p.ws.worker_first[2 * b] = make_int4(lo, p.ws.rec_prefix[lo], p.ws.rec_prefix[lo + 1], 0);
+        p.ws.worker_first[2 * b + 1] = p.ws.rec[lo];
     }
     // sequences without context: zero output (no private and no shared tiles)
     const int rowlen = p.num_q_heads * p.head_dim;
@@ -529,16 +536,20 @@ struct RecCursor {
     int gbase;                  // private record: first tile of its group's record, or -1
 };
 
-__device__ __forceinline__ void rec_load(const DecodeParams& p, RecCursor& rc) {
-    rc.lo = __ldcg(&p.ws.rec_prefix[rc.r]);
-    rc.hi = __ldcg(&p.ws.rec_prefix[rc.r + 1]);
-    const int4 e = __ldcg(&p.ws.rec[rc.r]);
+__device__ __forceinline__ void rec_set(RecCursor& rc, int lo, int hi, int4 e) {
+    rc.lo = lo;
+    rc.hi = hi;
     rc.group = (e.x & kGroupRecord) != 0;
     rc.id = e.x & (kGroupRecord - 1);
     rc.start = e.y;
     rc.end = e.z;
     rc.members = rc.group ? e.w : 1;
     rc.gbase = rc.group ? -1 : e.w;
+}
+
+__device__ __forceinline__ void rec_load(const DecodeParams& p, RecCursor& rc) {
+    rec_set(rc, __ldcg(&p.ws.rec_prefix[rc.r]), __ldcg(&p.ws.rec_prefix[rc.r + 1]),
+            __ldcg(&p.ws.rec[rc.r]));
 }
 
 // The window starting at flattened tile `pos` of a worker whose range is
@@ -642,8 +653,13 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         uint32_t phase = 0;
         bool ok = true;
         RecCursor rc{};
-        rc.r = a < end ? p.ws.worker_rec[blockIdx.x] : 0;
-        if (a < end) rec_load(p, rc);
+        if (a < end) {
+            // the planner stored this worker's first record beside its index
+            const int4 wf = __ldcg(&p.ws.worker_first[2 * blockIdx.x]);
+            const int4 e = __ldcg(&p.ws.worker_first[2 * blockIdx.x + 1]);
+            rc.r = wf.x;
+            rec_set(rc, wf.y, wf.z, e);
+        }
         Window win = make_window(p, blockIdx.x, a, end, q, a, rc);
         int pos = a;
         int e0 = 0, e1 = 0;

@@ -44,9 +44,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # single-chunk contexts need no partial states
+    # single-chunk contexts need no partial states: the workspace is the fixed
+    # per-worker table (32 B x 4096 workers) plus small per-sequence arrays
     small = binding.pkv_decode_workspace_bytes(4, 8, 8, 64, 16, 256, "f32")
-    assert 0 < small < 64 * 1024
+    assert 0 < small < 192 * 1024
     # OPT-13B-shaped: 2048 tokens -> 4 chunks of 512 -> partial states for 64*40*4 chunks
     ws = binding.pkv_decode_workspace_bytes(64, 40, 40, 128, 16, 2048, "f16")
     assert ws >= 64 * 40 * 4 * (128 + 2) * 4
