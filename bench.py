@@ -53,6 +53,10 @@ def parse_args(argv=None):
                     help="measure pkv_swap_blocks (device pool <-> pinned host pool) instead")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="store the DRAM bytes per decode launch of an ncu --csv capture "
+                         "(dram__bytes_read.sum, dram__bytes_write.sum of decode_mma / "
+                         "decode_simt launches) for --workload in profiles/decode_traffic.json")
     return ap.parse_args(argv)
 
 
@@ -219,6 +223,35 @@ def recorded_traffic(workload: int):
     return rec.get("dram_bytes_per_launch")
 
 
+def record_traffic(csv_path: str, workload: int) -> dict:
+    """Average DRAM bytes (read + write) per decode launch of an ncu --csv log,
+    stored for `workload` with the hash of the decode sources it was taken on."""
+    import csv
+    rows = list(csv.reader(line for line in open(csv_path) if line.startswith('"')))
+    hdr = rows[0]
+    ki, mi, vi, ii, ui = (hdr.index(k) for k in ("Kernel Name", "Metric Name", "Metric Value",
+                                                  "ID", "Metric Unit"))
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+             "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    per = {}
+    for r in rows[1:]:
+        if "decode_mma_kernel" not in r[ki] and "decode_simt_kernel" not in r[ki]:
+            continue
+        if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            per.setdefault(r[ii], 0.0)
+            per[r[ii]] += float(r[vi].replace(",", "")) * scale[r[ui]]
+    if not per:
+        raise SystemExit(f"no decode launch with DRAM byte counters in {csv_path}")
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    d = json.load(open(path)) if os.path.exists(path) else {}
+    d[str(workload)] = {"dram_bytes_per_launch": sum(per.values()) / len(per),
+                        "launches": len(per), "source_hash": decode_source_hash()}
+    with open(path, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return d[str(workload)]
+
+
 # ------------------------------------------------------------ CPU baseline --
 
 def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int = 0,
@@ -282,7 +315,11 @@ def run_ours(args, rank, world, local):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = w.kv_read_bytes < 4 * l2
     flush_buf = torch.empty(2 * l2 // 4 * 4 if flush else 4, dtype=torch.uint8, device=device)
-    launches_per_step = (1 if len(w.step_pairs) else 0) + 1 + 2   # copy, append, plan+decode
+    # copy (if any), append, then plan + decode (+ the merge kernel of a grouped launch on
+    # the tensor-core path: 16-bit q with K/V of the same type, or e4m3 K/V at d = 128)
+    mma = w.q_dtype in ("f16", "bf16") and (w.kv_dtype == w.q_dtype or
+                                             (w.kv_dtype == "e4m3" and w.head_dim == 128))
+    launches_per_step = (1 if len(w.step_pairs) else 0) + 1 + 2 + (1 if mma and st.prefix else 0)
 
     def step_with_decode_events(dec0, dec1):
         st.copy_step(stream)
@@ -352,6 +389,9 @@ def run_ours(args, rank, world, local):
     dec_s = float(np.mean(dec_ms)) * 1e-3
     achieved = w.kv_read_bytes / dec_s / 1e9
     copy_peak = copy_peak_gbs(torch, device, stream) if rank == 0 else None
+    # DRAM bytes of one decode launch from the committed ncu capture (when it was taken
+    # on this source): the shared-prefix workload reads far fewer bytes than it attends
+    traffic = recorded_traffic(args.workload) if args.num_seqs is None else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(slowest * 1e3, 5),
@@ -364,13 +404,15 @@ def run_ours(args, rank, world, local):
             "block_size": w.block_size, "kv_dtype": w.kv_dtype,
             "mean_context": float(w.context_lens.mean()),
             "kv_read_bytes_per_step": w.kv_read_bytes,
+            "unique_kv_bytes_per_step": w.unique_kv_bytes,
             "l2": ("L2 flushed between steps (write of 2x L2)" if flush else
                    f"inputs larger than L2 ({w.kv_read_bytes / 1e9:.2f} GB of KV per step)"),
             "step": "copy_blocks (if any) + reshape_and_cache + paged decode",
             "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(args.workload),
+                     "traffic": traffic,
+                     "dram_gbs": round(traffic / dec_s / 1e9, 1) if traffic else None,
                      "kernel": "planning + decode kernels (CUDA events around the decode call)",
                      "decode_us": round(dec_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -468,7 +510,9 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
-    if args.swap:
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload)))
+    elif args.swap:
         run_swap(args, rank, world, local)
     elif args.impl == "reference":
         run_reference(args, rank, world, local)

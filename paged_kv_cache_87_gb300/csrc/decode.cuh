@@ -81,7 +81,8 @@ struct DecodeParams {
     int chunk_tokens, max_chunks;
     int part_stride;      // partial states per (sequence, query head) in the workspace
     int num_workers;      // CTAs of the balanced-split decode
-    int allow_groups;     // group sequences that share leading blocks (prefix-aware decode)
+    int allow_groups;     // group sequences that share leading blocks (prefix-aware decode);
+                          // its split units are merged by a separate merge kernel
     float qk_scale_log2;  // scale * log2(e) (* kv_scale for FP8)
     float out_scale;      // kv_scale for FP8, else 1
 };

@@ -80,6 +80,10 @@ cudaError_t launch_decode_mma_nt(const DecodeParams& p, cudaStream_t stream) {
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     kernel<<<ps.num_workers, Cfg::THREADS, Cfg::SMEM, stream>>>(ps, tk, tv);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || !ps.allow_groups) return err;
+    const int units = ps.num_seqs * ps.num_kv_heads * ps.nsub;
+    merge_units_kernel<QT, HD><<<(units + 7) / 8, 256, 0, stream>>>(ps);
     return cudaGetLastError();
 }
 

@@ -399,25 +399,7 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         p.ws.quota[0] = q;
         p.ws.quota[1] = total;
     }
-    // partial states each unit of a grouped sequence merges: its group's shared
-    // segments, then its private ones (private units carry the count in their
-    // work record's window instead)
     const bool in_smem = p.num_seqs <= (int)blockDim.x;
-    if (can_group) {
-        for (int idx = tid; idx < p.num_seqs * upi; idx += blockDim.x) {
-            const int s = idx / upi, u = idx % upi;
-            const int4 si = in_smem ? make_int4(s_run[s], s_ctx[s], s_mem[s], s_sh[s])
-                                    : p.ws.seq_info[s];
-            if (si.z < 0) continue;                        // not in a group
-            int np = 0;
-            if (si.x > 0) {
-                const int us = si.y + u * si.x;
-                np = (us + si.x - 1) / q - us / q + 1;
-            }
-            const int gs = si.z + u * si.w;
-            p.ws.unit_expect[idx] = (gs + si.w - 1) / q - gs / q + 1 + np;
-        }
-    }
     __syncthreads();
     // each worker's first record: the last record starting at or before its first
     // tile (binary search over the record prefix)
@@ -511,6 +493,38 @@ __device__ __noinline__ void merge_rows_warp(const DecodeParams& p, int64_t row,
         store_from_float<QT>(p.out, o0 + 4 * k + 2, A[k].z * inv);
         store_from_float<QT>(p.out, o0 + 4 * k + 3, A[k].w * inv);
     }
+}
+
+// Grouped (prefix-aware) launches: after the decode kernel, one warp per
+// (sequence, unit) merges the unit's partial states -- its group's shared
+// segments, then its private ones, in that order -- all units in parallel.
+// Ungrouped units whose context fits one segment were written directly.
+template <typename QT, int HD>
+__global__ void __launch_bounds__(256) merge_units_kernel(DecodeParams p) {
+    const int upi = p.num_kv_heads * p.nsub;
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= p.num_seqs * upi) return;
+    const int s = w / upi, u = w % upi;
+    const int q = p.ws.quota[0];
+    const int4 si = p.ws.seq_info[s];   // {private tiles, first private tile, group base, group tiles}
+    int np = 0, ns = 0;
+    if (si.x > 0) {
+        const int us = si.y + u * si.x;
+        np = (us + si.x - 1) / q - us / q + 1;
+    }
+    if (si.z >= 0) {
+        const int gs = si.z + u * si.w;
+        ns = (gs + si.w - 1) / q - gs / q + 1;
+    }
+    const int nseg = ns + np;
+    if (nseg == 0 || (si.z < 0 && nseg == 1)) return;
+    const int kvh = u / p.nsub, qsub = u % p.nsub;
+    const int nh = min(kMmaHeadsPerItem, p.group - qsub * kMmaHeadsPerItem);
+    const int hs = lane >> 2;
+    const int64_t row = hs < nh ? (int64_t)s * p.num_q_heads + kvh * p.group +
+                                      qsub * kMmaHeadsPerItem + hs
+                                : -1;
+    merge_rows_warp<QT, HD>(p, row, nseg, lane);
 }
 
 // ------------------------------------------------------------ work windows --
@@ -757,6 +771,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     }
 
     // ========================= consumer warp =========================
+    const bool grp_launch = p.allow_groups != 0;   // merges left to the merge kernel
     const int g = lane >> 2, c = lane & 3;
     uint32_t qf[NT][Cfg::KSTEPS][2];   // Q^T B fragments, n-tile nt = head slots 8nt..8nt+7
     float o[Cfg::MTILES][NT][4];       // O^T C fragments, rows mapped to d by d_row()
@@ -998,8 +1013,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 if (j >= meta.nh) continue;
                 int seq, qh;
                 slot_head(p, grp, meta.s, meta.kvh, meta.qsub, j, &seq, &qh);
-                const int expect =
-                    grp ? __ldcg(&p.ws.unit_expect[seq * upi + meta.kvh]) : meta.expect;
+                const int expect = grp ? 0 : meta.expect;   // grouped: always a partial state
                 const int64_t sh = (int64_t)seq * p.num_q_heads + qh;
                 const float lsum = hh ? l1[nt] : l0[nt];
                 const float msum = hh ? m1[nt] : m0[nt];
@@ -1029,39 +1043,25 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         }
         // split units: lane i (< units served) arrives on unit i's counter once the
         // warp barrier has ordered every lane's partial-state stores before it;
-        // units the segment covers whole need neither
+        // units the segment covers whole need neither.  Grouped launches leave
+        // every merge to the merge kernel.
         __syncwarp();
-        const int nunits = grp ? meta.nchunks : 1;   // members served
-        int my_expect = 1;
+        if (grp_launch) continue;
+        const int my_expect = meta.expect;
         bool last = false;
-        if (lane < nunits) {
-            const int unit = (meta.s + (grp ? lane : 0)) * upi + meta.kvh * p.nsub + meta.qsub;
-            my_expect = grp ? __ldcg(&p.ws.unit_expect[unit]) : meta.expect;
-            if (my_expect > 1)
-                last = atom_add_acq_rel_gpu(&p.ws.unit_done[unit], 1u) ==
-                       (unsigned)(my_expect - 1);
+        if (lane == 0 && my_expect > 1) {
+            const int unit = meta.s * upi + meta.kvh * p.nsub + meta.qsub;
+            last = atom_add_acq_rel_gpu(&p.ws.unit_done[unit], 1u) == (unsigned)(my_expect - 1);
         }
         unsigned last_mask = __ballot_sync(0xffffffffu, last);
-        if (last_mask) __syncwarp();   // the acquiring lanes' view reaches the warp
-        // merges of the units this warp finished last, whole units, <= 8 heads a pass
-        const int nh_unit = grp ? p.group : meta.nh;
-        while (last_mask) {
-            int64_t row = -1;
-            int nseg = 0, used = 0;
-            while (last_mask && used + nh_unit <= 8) {
-                const int i = __ffs(last_mask) - 1;
-                last_mask &= last_mask - 1;
-                const int n_i = __shfl_sync(0xffffffffu, my_expect, i);
-                const int hs = (lane >> 2) - used;
-                if (hs >= 0 && hs < nh_unit) {
-                    const int seq = meta.s + (grp ? i : 0);
-                    const int hq0 = meta.kvh * p.group + (grp ? 0 : meta.qsub * kMmaHeadsPerItem);
-                    row = (int64_t)seq * p.num_q_heads + hq0 + hs;
-                    nseg = n_i;
-                }
-                used += nh_unit;
-            }
-            merge_rows_warp<QT, HD>(p, row, nseg, lane);
+        if (last_mask) __syncwarp();   // the acquiring lane's view reaches the warp
+        // the merge of the unit this warp finished last
+        if (last_mask) {
+            const int hs = lane >> 2;
+            const int64_t row = hs < meta.nh ? (int64_t)meta.s * p.num_q_heads + meta.kvh * p.group +
+                                                   meta.qsub * kMmaHeadsPerItem + hs
+                                             : -1;
+            merge_rows_warp<QT, HD>(p, row, my_expect, lane);
         }
     }
 }
