@@ -425,73 +425,90 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
     }
 }
 
-// Merge of the partial states of up to 8 (sequence, query head) rows, one
-// row per 4 lanes (lane 4h + q holds quarter q of d of row h): M = max m_c,
-// L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L over the row's
-// nseg states, in state order.  Lanes with row < 0 idle.  Loads of several
-// states are issued together: the states sit in L2, written by other CTAs.
-template <typename QT, int HD>
+// Merge of the partial states of up to 32 / LPR (sequence, query head) rows,
+// LPR lanes per row (lane LPR*h + k holds slice k of d of row h): M = max m_c,
+// L = sum l_c 2^(m_c - M), out = sum acc_c 2^(m_c - M) / L over the row's nseg
+// states, in state order.  Lanes with row < 0 idle.  The states sit in L2,
+// written by other CTAs: a batch of states is loaded at once, and a row with
+// more states than a batch carries M forward batch by batch (the earlier sums
+// rescaled by 2^(M_old - M_new)).
+template <typename QT, int HD, int LPR>
 __device__ __noinline__ void merge_rows_warp(const DecodeParams& p, int64_t row, int nseg,
                                              int lane) {
-    constexpr int DQ = HD / 4;     // dims per lane: 32 or 16
-    constexpr int NV = DQ / 4;     // float4 per lane and state
+    constexpr int DQ = HD / LPR;               // dims per lane
+    constexpr int NV = DQ / 4;                 // float4 per lane and state
+    constexpr int NB = NV >= 8 ? 2 : 16 / NV;  // states per batch (<= 16 float4 in flight)
     if (row < 0) return;
-    const int q4 = lane & 3;
+    const int k = lane % LPR;
     const float* pm = p.ws.pm + row * p.part_stride;
     const float* pl = p.ws.pl + row * p.part_stride;
     const float4* pa = reinterpret_cast<const float4*>(p.ws.pacc + row * p.part_stride * HD) +
-                       q4 * NV;
-    float M = -INFINITY;
-    int c = 0;
-    for (; c + 4 <= nseg; c += 4) {
-        const float a0 = __ldcg(pm + c), a1 = __ldcg(pm + c + 1);
-        const float a2 = __ldcg(pm + c + 2), a3 = __ldcg(pm + c + 3);
-        M = fmaxf(M, fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)));
-    }
-    for (; c < nseg; ++c) M = fmaxf(M, __ldcg(pm + c));
-    float L = 0.f;
+                       k * NV;
+    float M = -INFINITY, L = 0.f;
     float4 A[NV];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) A[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    auto add = [&](const float4 (&v)[NV], float mc, float lc) {
-        const float f = mc == -INFINITY ? 0.f : fast_exp2(mc - M);
-        L = fmaf(lc, f, L);
+    for (int i = 0; i < NV; ++i) A[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < nseg; c0 += NB) {
+        float mb[NB], lb[NB];
+        float4 v[NB][NV];
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            A[k].x = fmaf(v[k].x, f, A[k].x);
-            A[k].y = fmaf(v[k].y, f, A[k].y);
-            A[k].z = fmaf(v[k].z, f, A[k].z);
-            A[k].w = fmaf(v[k].w, f, A[k].w);
+        for (int b = 0; b < NB; ++b) {
+            const bool in = c0 + b < nseg;
+            mb[b] = in ? __ldcg(pm + c0 + b) : -INFINITY;
+            lb[b] = in ? __ldcg(pl + c0 + b) : 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                v[b][i] = in ? __ldcg(pa + (int64_t)(c0 + b) * (HD / 4) + i)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-    };
-    c = 0;
-    for (; c + 2 <= nseg; c += 2) {
-        float4 v0[NV], v1[NV];
-        const float m0 = __ldcg(pm + c), m1 = __ldcg(pm + c + 1);
-        const float l0 = __ldcg(pl + c), l1 = __ldcg(pl + c + 1);
+        float Mn = M;
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            v0[k] = __ldcg(pa + (int64_t)c * (HD / 4) + k);
-            v1[k] = __ldcg(pa + (int64_t)(c + 1) * (HD / 4) + k);
+        for (int b = 0; b < NB; ++b) Mn = fmaxf(Mn, mb[b]);
+        if (Mn == -INFINITY) continue;
+        if (M != Mn && M != -INFINITY) {
+            const float r = fast_exp2(M - Mn);
+            L *= r;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                A[i].x *= r; A[i].y *= r; A[i].z *= r; A[i].w *= r;
+            }
         }
-        add(v0, m0, l0);
-        add(v1, m1, l1);
-    }
-    if (c < nseg) {
-        float4 v0[NV];
-        const float m0 = __ldcg(pm + c), l0 = __ldcg(pl + c);
+        M = Mn;
 #pragma unroll
-        for (int k = 0; k < NV; ++k) v0[k] = __ldcg(pa + (int64_t)c * (HD / 4) + k);
-        add(v0, m0, l0);
+        for (int b = 0; b < NB; ++b) {
+            const float f = mb[b] == -INFINITY ? 0.f : fast_exp2(mb[b] - M);
+            L = fmaf(lb[b], f, L);
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                A[i].x = fmaf(v[b][i].x, f, A[i].x);
+                A[i].y = fmaf(v[b][i].y, f, A[i].y);
+                A[i].z = fmaf(v[b][i].z, f, A[i].z);
+                A[i].w = fmaf(v[b][i].w, f, A[i].w);
+            }
+        }
     }
     const float inv = L > 0.f ? p.out_scale / L : 0.f;
-    const int64_t o0 = row * HD + q4 * DQ;
+    const int64_t o0 = row * HD + k * DQ;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        store_from_float<QT>(p.out, o0 + 4 * k + 0, A[k].x * inv);
-        store_from_float<QT>(p.out, o0 + 4 * k + 1, A[k].y * inv);
-        store_from_float<QT>(p.out, o0 + 4 * k + 2, A[k].z * inv);
-        store_from_float<QT>(p.out, o0 + 4 * k + 3, A[k].w * inv);
+    for (int i = 0; i < NV; ++i) {
+        store_from_float<QT>(p.out, o0 + 4 * i + 0, A[i].x * inv);
+        store_from_float<QT>(p.out, o0 + 4 * i + 1, A[i].y * inv);
+        store_from_float<QT>(p.out, o0 + 4 * i + 2, A[i].z * inv);
+        store_from_float<QT>(p.out, o0 + 4 * i + 3, A[i].w * inv);
+    }
+}
+
+// The merge of the nh (<= 8) heads of one unit by a warp: 8 lanes per row when
+// the unit has at most 4 heads, else 4.
+template <typename QT, int HD>
+__device__ __forceinline__ void merge_unit_warp(const DecodeParams& p, int64_t row0, int nh,
+                                                int nseg, int lane) {
+    if (nh <= 4) {
+        const int h = lane >> 3;
+        merge_rows_warp<QT, HD, 8>(p, h < nh ? row0 + h : -1, nseg, lane);
+    } else {
+        const int h = lane >> 2;
+        merge_rows_warp<QT, HD, 4>(p, h < nh ? row0 + h : -1, nseg, lane);
     }
 }
 
@@ -520,11 +537,8 @@ __global__ void __launch_bounds__(256) merge_units_kernel(DecodeParams p) {
     if (nseg == 0 || (si.z < 0 && nseg == 1)) return;
     const int kvh = u / p.nsub, qsub = u % p.nsub;
     const int nh = min(kMmaHeadsPerItem, p.group - qsub * kMmaHeadsPerItem);
-    const int hs = lane >> 2;
-    const int64_t row = hs < nh ? (int64_t)s * p.num_q_heads + kvh * p.group +
-                                      qsub * kMmaHeadsPerItem + hs
-                                : -1;
-    merge_rows_warp<QT, HD>(p, row, nseg, lane);
+    merge_unit_warp<QT, HD>(p, (int64_t)s * p.num_q_heads + kvh * p.group +
+                                   qsub * kMmaHeadsPerItem, nh, nseg, lane);
 }
 
 // ------------------------------------------------------------ work windows --
@@ -1056,13 +1070,9 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         unsigned last_mask = __ballot_sync(0xffffffffu, last);
         if (last_mask) __syncwarp();   // the acquiring lane's view reaches the warp
         // the merge of the unit this warp finished last
-        if (last_mask) {
-            const int hs = lane >> 2;
-            const int64_t row = hs < meta.nh ? (int64_t)meta.s * p.num_q_heads + meta.kvh * p.group +
-                                                   meta.qsub * kMmaHeadsPerItem + hs
-                                             : -1;
-            merge_rows_warp<QT, HD>(p, row, my_expect, lane);
-        }
+        if (last_mask)
+            merge_unit_warp<QT, HD>(p, (int64_t)meta.s * p.num_q_heads + meta.kvh * p.group +
+                                           meta.qsub * kMmaHeadsPerItem, meta.nh, my_expect, lane);
     }
 }
 
