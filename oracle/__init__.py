@@ -76,6 +76,10 @@ def _load():
         lib.oracle_attention_partial.restype = i32
         lib.oracle_merge_partials.argtypes = [i32, P, P, P, i32, P]
         lib.oracle_merge_partials.restype = None
+        lib.oracle_paged_prefill_attention.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32,
+                                                       i32, i32, i32, f64, i32, i32, f64, P,
+                                                       i32, P, i32]
+        lib.oracle_paged_prefill_attention.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -185,6 +189,39 @@ def attention_partial(query, k_cache, v_cache, block_tables, *, num_q_heads, num
     if rc != 0:
         raise ValueError("oracle attention_partial: block id out of range")
     return float(m[0]), float(l[0]), acc
+
+
+def paged_prefill_attention(query, k_cache, v_cache, block_tables, context_lens, query_start,
+                            *, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                            scale, q_dtype, kv_dtype, kv_scale=1.0, sel=None,
+                            nthreads=1) -> np.ndarray:
+    """fp64 causal multi-query outputs for the (query row, q head) pairs in ``sel``.
+
+    Query row r of sequence s (query_start[s] <= r < query_start[s+1]) sits at
+    position context_lens[s] - n_s + (r - query_start[s]) and attends to every
+    token up to and including it.  Returns [len(sel), head_dim], or
+    [total_q, Hq, d] when ``sel`` is None.
+    """
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    S = context_lens.shape[0]
+    total_q = int(query_start[-1])
+    full = sel is None
+    if full:
+        sel = np.stack(np.meshgrid(np.arange(total_q), np.arange(num_q_heads), indexing="ij"),
+                       -1).reshape(-1, 2)
+    sel = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
+    out = np.zeros((sel.shape[0], head_dim), dtype=np.float64)
+    rc = _load().oracle_paged_prefill_attention(
+        _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start), S, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+        int(block_tables.shape[1]), float(scale), _code(q_dtype), _code(kv_dtype),
+        float(kv_scale), _ptr(sel), int(sel.shape[0]), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle paged_prefill_attention: bad argument, more queries than "
+                         "context, or block id out of range")
+    return out.reshape(total_q, num_q_heads, head_dim) if full else out
 
 
 def merge_partials(ms, ls, accs) -> np.ndarray:

@@ -220,13 +220,14 @@ static int fetch_row(const dec_args* a, const void* cache, int s, int g, int t, 
     return 0;
 }
 
-/* Unnormalised attention state over logical tokens [t0, t1) of (s, h):
+/* Unnormalised attention state over logical tokens [t0, t1) of sequence s for
+ * query head h of query row `qrow` (the sequence's own row for decode):
  *   z_t = scale * q.k_t,  m = max z_t,  l = sum exp(z_t - m),
  *   acc = sum exp(z_t - m) v_t.
  * The full output is acc / l ([P1] §3: a_ij = exp(z_j) / sum_t exp(z_t),
  * o_i = sum_j a_ij v_j; subtracting m from every logit leaves a_ij unchanged).
  * An empty range gives m = -inf, l = 0, acc = 0. */
-static int partial_state(const dec_args* a, int s, int h, int t0, int t1,
+static int partial_state(const dec_args* a, int s, int qrow, int h, int t0, int t1,
                          double* m_out, double* l_out, double* acc) {
     int d = a->head_dim;
     int g = h / (a->num_q_heads / a->num_kv_heads);
@@ -240,7 +241,7 @@ static int partial_state(const dec_args* a, int s, int h, int t0, int t1,
     double* z = malloc(sizeof(double) * n);
     int rc = 0;
     for (int i = 0; i < d; ++i)
-        q[i] = load_elem(a->query, a->q_dtype, ((int64_t)s * a->num_q_heads + h) * d + i);
+        q[i] = load_elem(a->query, a->q_dtype, ((int64_t)qrow * a->num_q_heads + h) * d + i);
     /* pass 1: logits, [P1] §3 S_ij = q^T K_j^T / sqrt(d) (scale passed in) */
     double m = -INFINITY;
     for (int t = t0; t < t1 && !rc; ++t) {
@@ -306,7 +307,7 @@ int oracle_paged_decode_attention(const void* query, const void* k_cache, const 
         double m, l;
         double* o = out + (int64_t)k * head_dim;
         if (ctx > max_blocks * block_size) { bad = 1; continue; }
-        if (partial_state(&a, s, h, 0, ctx, &m, &l, o)) { bad = 1; continue; }
+        if (partial_state(&a, s, s, h, 0, ctx, &m, &l, o)) { bad = 1; continue; }
         if (ctx == 0) continue;                          /* zeros */
         for (int i = 0; i < head_dim; ++i) o[i] /= l;
     }
@@ -327,7 +328,7 @@ int oracle_attention_partial(const void* query, const void* k_cache, const void*
     dec_args a;
     fill_args(&a, query, k_cache, v_cache, block_tables, NULL, num_q_heads, num_kv_heads,
               head_dim, block_size, num_blocks, max_blocks, scale, q_dtype, kv_dtype, kv_scale);
-    return partial_state(&a, seq, q_head, t0, t1, m, l, acc);
+    return partial_state(&a, seq, seq, q_head, t0, t1, m, l, acc);
 }
 
 /*
@@ -351,6 +352,56 @@ void oracle_merge_partials(int n, const double* ms, const double* ls, const doub
         for (int i = 0; i < head_dim; ++i) out[i] += accs[(int64_t)k * head_dim + i] * f;
     }
     for (int i = 0; i < head_dim; ++i) out[i] /= l;
+}
+
+/* ------------------- multi-query paged attention ([P1] §1, §3) ----------- */
+
+/*
+ * Causal attention of several query tokens per sequence over the paged cache
+ * (prefill, chunked prefill, or verifying a chain of draft tokens).  Sequence s
+ * owns query rows query_start[s] .. query_start[s+1]-1 of `query`
+ * ([total_q, num_q_heads, head_dim]); its cache holds context_lens[s] >= n_s
+ * tokens, the last n_s of them being these queries' own keys and values.
+ * Query i of the sequence is the token at logical position p = ctx - n_s + i
+ * and, like every generated token in [P1] §1, attends to all tokens before it
+ * and to itself: o = softmax(scale * q K[0..p]^T) V[0..p] ([P1] §3), i.e. the
+ * decode attention of that row over the first p + 1 tokens.
+ * `sel` lists (query row, query head) pairs; out[k][:] gets pair k's output.
+ * Returns 0, or -1 on a bad argument, n_s > ctx_s, or a block id out of range.
+ */
+int oracle_paged_prefill_attention(const void* query, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, const int32_t* context_lens,
+                                   const int32_t* query_start, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   int max_blocks, double scale, int q_dtype, int kv_dtype,
+                                   double kv_scale, const int32_t* sel, int num_sel, double* out,
+                                   int nthreads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || num_seqs < 0) return -1;
+    if (!elem_bytes(q_dtype) || q_dtype == OR_E4M3 || !elem_bytes(kv_dtype)) return -1;
+    dec_args a;
+    fill_args(&a, query, k_cache, v_cache, block_tables, context_lens, num_q_heads,
+              num_kv_heads, head_dim, block_size, num_blocks, max_blocks, scale, q_dtype,
+              kv_dtype, kv_scale);
+    int bad = 0;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1) reduction(| : bad)
+    for (int k = 0; k < num_sel; ++k) {
+        int row = sel[2 * k], h = sel[2 * k + 1];
+        double* o = out + (int64_t)k * head_dim;
+        /* the sequence owning this query row */
+        int s = -1;
+        for (int j = 0; j < num_seqs; ++j)
+            if (query_start[j] <= row && row < query_start[j + 1]) { s = j; break; }
+        if (s < 0) { bad = 1; continue; }
+        int n = query_start[s + 1] - query_start[s];
+        int ctx = context_lens[s];
+        if (n > ctx || ctx > max_blocks * block_size) { bad = 1; continue; }
+        int p = ctx - n + (row - query_start[s]);        /* logical position of the query */
+        double m, l;
+        if (partial_state(&a, s, row, h, 0, p + 1, &m, &l, o)) { bad = 1; continue; }
+        for (int i = 0; i < head_dim; ++i) o[i] /= l;
+    }
+    return bad ? -1 : 0;
 }
 
 /* Threads the OpenMP runtime would give a parallel region (1 without OpenMP). */

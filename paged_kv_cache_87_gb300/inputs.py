@@ -398,5 +398,135 @@ def make_config(cid: int, *, num_seqs: int | None = None, ctx_cap: int | None = 
                             scale=1.0 / math.sqrt(128))
 
 
+# ----------------------------------------------------- multi-query inputs --
+
+@dataclass
+class MultiQueryWorkload:
+    """Several query tokens per sequence over a paged cache (prefill / chunked prefill).
+
+    Sequence s has prior[s] tokens cached before the step and n[s] new tokens;
+    the step writes the new tokens' K/V (rows ``new_idx`` at ``slots[new_idx]``)
+    and attends causally with their n[s] queries over ctx = prior + n tokens.
+    """
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    q_dtype: str
+    kv_dtype: str
+    scale: float
+    query: np.ndarray          # [total_q, Hq, d] storage
+    key: np.ndarray            # [T, Hkv, d] storage: every cached token's key
+    value: np.ndarray
+    slots: np.ndarray          # [T] int64 slot of each row
+    prior_idx: np.ndarray      # rows cached before the step
+    new_idx: np.ndarray        # rows the step writes (the queries' own tokens)
+    block_tables: np.ndarray   # int32 [S, max_blocks], -1 padded
+    context_lens: np.ndarray   # int32 [S] = prior + n
+    query_start: np.ndarray    # int32 [S + 1]
+    seq_tokens: list           # per sequence: its rows in position order
+
+    src_dtype = property(lambda self: self.kv_dtype)
+    kv_scale = property(lambda self: 1.0)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.query_start[-1])
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    @property
+    def cache_shape(self) -> tuple:
+        return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+    @property
+    def num_new(self) -> np.ndarray:
+        return np.diff(self.query_start.astype(np.int64))
+
+    @property
+    def flops(self) -> int:
+        """Causal attention FLOPs: 4 d Hq per (query, visible key) pair (Q K^T and P V)."""
+        n = self.num_new
+        prior = self.context_lens.astype(np.int64) - n
+        pairs = int((n * prior + n * (n + 1) // 2).sum())
+        return 4 * self.head_dim * self.num_q_heads * pairs
+
+    @property
+    def kv_bytes(self) -> int:
+        """K and V bytes of every cached token (each read at least once)."""
+        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * \
+            self.head_dim * DTYPE_BYTES[self.kv_dtype] * 2
+
+
+def make_multi_query(name: str, rng: np.random.Generator, prior, n, *, num_q_heads: int,
+                     num_kv_heads: int, head_dim: int = 128, block_size: int = 16,
+                     dtype: str = "bf16", scale: float | None = None,
+                     slack: float = 0.10) -> MultiQueryWorkload:
+    """Private blocks per sequence from a seeded permutation of the pool; q/K/V ~ N(0,1)."""
+    prior = np.asarray(prior, dtype=np.int64)
+    n = np.asarray(n, dtype=np.int64)
+    S = int(prior.shape[0])
+    ctx = prior + n
+    nblk = [-(-int(c) // block_size) for c in ctx]
+    num_blocks = max(4, math.ceil(sum(nblk) * (1.0 + slack)) + 2)
+    bm = BlockManager(num_blocks, block_size, rng)
+    tables = [bm.allocate(int(c)) for c in ctx]
+    T = int(ctx.sum())
+    offsets = np.concatenate([[0], np.cumsum(ctx)])
+    slots = np.empty(T, dtype=np.int64)
+    is_new = np.zeros(T, dtype=bool)
+    for s in range(S):
+        for p in range(int(ctx[s])):
+            slots[offsets[s] + p] = bm.slot(tables[s], p)
+        is_new[offsets[s] + prior[s]: offsets[s + 1]] = True
+    query_start = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    query = draw_normal(rng, (int(query_start[-1]), num_q_heads, head_dim), dtype)
+    key = draw_normal(rng, (T, num_kv_heads, head_dim), dtype)
+    value = draw_normal(rng, (T, num_kv_heads, head_dim), dtype)
+    return MultiQueryWorkload(
+        name=name, num_seqs=S, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=block_size, num_blocks=num_blocks, q_dtype=dtype,
+        kv_dtype=dtype, scale=scale if scale is not None else 1.0 / math.sqrt(head_dim),
+        query=query, key=key, value=value, slots=slots,
+        prior_idx=np.nonzero(~is_new)[0], new_idx=np.nonzero(is_new)[0],
+        block_tables=_pack_tables(tables), context_lens=ctx.astype(np.int32),
+        query_start=query_start,
+        seq_tokens=[np.arange(offsets[s], offsets[s + 1]) for s in range(S)])
+
+
+MQ_CONFIG_NAMES = {
+    0: "multi-query mix: 5 seqs, 8q/2kv heads, d128, bf16, B16, prior {0..300} + 1..200 queries",
+    1: "chunked prefill: 16 seqs, 32q/8kv heads, d128, bf16, B16, prior U[0,8192] + 512 queries",
+    2: "prefill MHA: 4 seqs, 16 heads, d128, fp16, B16, prompts U[1024,4096], no prior context",
+}
+
+
+def make_multi_query_config(cid: int, *, seed: int | None = None) -> MultiQueryWorkload:
+    """The seeded multi-query workloads (seed 8790 + id)."""
+    rng = np.random.default_rng(8790 + cid if seed is None else seed)
+    name = MQ_CONFIG_NAMES[cid]
+    if cid == 0:
+        return make_multi_query(name, rng, [0, 37, 300, 5, 129], [1, 64, 200, 130, 33],
+                                num_q_heads=8, num_kv_heads=2)
+    if cid == 1:
+        prior = rng.integers(0, 8192 + 1, size=16)
+        return make_multi_query(name, rng, prior, np.full(16, 512), num_q_heads=32,
+                                num_kv_heads=8)
+    if cid == 2:
+        n = rng.integers(1024, 4096 + 1, size=4)
+        return make_multi_query(name, rng, np.zeros(4, np.int64), n, num_q_heads=16,
+                                num_kv_heads=16, dtype="f16")
+    raise ValueError(f"no multi-query workload {cid}")
+
+
 def seeded_rng(seed: int) -> np.random.Generator:
     return np.random.default_rng(seed)
