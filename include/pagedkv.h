@@ -166,6 +166,50 @@ PKV_API pkv_status pkv_paged_decode_attention_prefix(
     size_t workspace_bytes, void* out, pkv_stream_t stream);
 
 /*
+ * Multi-query (causal) paged attention: several query tokens per sequence --
+ * prefill, chunked prefill, or the verification of a chain of draft tokens
+ * ("...Mathematical Foundations" §1 The Prefill (Prompt) Phase: a prompt's
+ * tokens are processed in parallel as dense tensor-core products, and a token
+ * attends to every earlier token and itself; §3 o = softmax(q K^T / sqrt(d)) V
+ * through the block table).
+ *
+ * Sequence s owns query rows query_start[s] .. query_start[s+1]-1 (n_s rows);
+ * its cache holds context_lens[s] >= n_s tokens, the last n_s being the
+ * queries' own keys and values (written beforehand, e.g. by
+ * pkv_reshape_and_cache).  Query row query_start[s] + i is the token at
+ * position p = context_lens[s] - n_s + i; for each query head h
+ *   out[row][h][:] = softmax_t(scale * q[row][h] . k_t) v_t over t = 0 .. p,
+ * k_t / v_t of kv head h / (num_q_heads / num_kv_heads) found through the
+ * table as in pkv_paged_decode_attention.
+ *
+ *   query        [total_q][num_q_heads][head_dim], q_dtype, 16-byte aligned
+ *   query_start  device int32 [num_seqs + 1], query_start[0] = 0,
+ *                non-decreasing, query_start[num_seqs] = total_q
+ *   context_lens device int32 [num_seqs], n_s <= context_lens[s] <= the table's
+ *                capacity; a sequence breaking this is skipped (its rows are
+ *                left untouched) and flagged PKV_DEV_BAD_CONTEXT
+ *   workspace    >= pkv_multi_query_workspace_bytes(num_seqs), 256-byte aligned
+ *   out          [total_q][num_q_heads][head_dim], q_dtype, 16-byte aligned
+ *   other arguments as in pkv_paged_decode_attention.
+ * Supported: q_dtype PKV_F16 or PKV_BF16 with kv_dtype == q_dtype,
+ * head_dim 128, block_size in {8, 16, 32}, num_q_heads / num_kv_heads a
+ * divisor of 128; others return PKV_ERR_UNSUPPORTED.  Q K^T and P V run on the
+ * tcgen05 tensor cores with fp32 accumulation in tensor memory; P is rounded
+ * to q_dtype before P V (the softmax denominator sums the rounded weights).
+ * Two launches on `stream`: a one-CTA planning kernel and the attention
+ * kernel (one CTA per sequence, kv head and 128 (query, head) rows).
+ */
+PKV_API size_t pkv_multi_query_workspace_bytes(int num_seqs);
+
+PKV_API pkv_status pkv_paged_multi_query_attention(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* query_start, int num_seqs, int total_q,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
+    pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
+    pkv_stream_t stream);
+
+/*
  * Write new tokens' keys and values into their cache slots
  * ("...Mathematical Foundations" §7 kernel 1; §4 Allocation Lifecycle step 2).
  *

@@ -44,6 +44,13 @@ _SIGNATURES = {
                                                      ctypes.c_float, ctypes.c_void_p,
                                                      ctypes.c_size_t, ctypes.c_void_p,
                                                      ctypes.c_void_p]),
+    "pkv_multi_query_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int]),
+    "pkv_paged_multi_query_attention": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 6 + [ctypes.c_int] * 9 + [ctypes.c_float, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_float,
+                                                      ctypes.c_void_p, ctypes.c_size_t,
+                                                      ctypes.c_void_p, ctypes.c_void_p]),
     "pkv_paged_decode_attention_noalloc": (
         ctypes.c_int,
         [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
@@ -193,6 +200,56 @@ def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cac
         int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
     _check(fn, st)
+    return out
+
+
+def pkv_multi_query_workspace_bytes(num_seqs: int) -> int:
+    return int(load().pkv_multi_query_workspace_bytes(int(num_seqs)))
+
+
+def pkv_paged_multi_query_attention(query: torch.Tensor, k_cache: torch.Tensor,
+                                    v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                    context_lens: torch.Tensor, query_start: torch.Tensor,
+                                    max_context_len: int, scale: float, kv_scale: float = 1.0,
+                                    workspace: torch.Tensor | None = None,
+                                    out: torch.Tensor | None = None,
+                                    stream=None) -> torch.Tensor:
+    """Causal attention of several query tokens per sequence over the paged cache.
+
+    query [total_q, Hq, d]; query_start int32 [S + 1] (rows of sequence s are
+    query_start[s] .. query_start[s+1]-1; query_start[S] = total_q);
+    context_lens int32 [S] counts the cached tokens including the queries'
+    own (the last n_s).  Row i of sequence s attends to tokens
+    0 .. context_lens[s] - n_s + i.
+    """
+    total_q, Hq, d = query.shape
+    NB, Hkv, B, d2 = k_cache.shape
+    S = int(context_lens.shape[0])
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("cache shapes must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or \
+            query_start.dtype != torch.int32:
+        raise ValueError("block_tables, context_lens and query_start must be int32")
+    if int(query_start.shape[0]) != S + 1:
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    for t, n in ((query, "query"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (query_start, "query_start")):
+        _cuda(t, n)
+    need = pkv_multi_query_workspace_bytes(S)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=query.device)
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _cuda(workspace, "workspace")
+    st = load().pkv_paged_multi_query_attention(
+        query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), query_start.data_ptr(), S, total_q, Hq, Hkv, d, B, NB,
+        block_tables.shape[1], int(max_context_len), float(scale), dtype_code(query),
+        dtype_code(k_cache), float(kv_scale), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
+    _check("pkv_paged_multi_query_attention", st)
     return out
 
 

@@ -7,6 +7,7 @@
 
 #include "cache_ops.cuh"
 #include "decode_launch.cuh"
+#include "mq_attention.cuh"
 
 // Per-device status word written by the kernels (bit-or of PKV_DEV_*).
 __device__ unsigned int g_pkv_status = 0u;
@@ -370,5 +371,69 @@ const char* pkv_status_string(pkv_status status) {
 }
 
 int pkv_version(void) { return 100; }
+
+
+size_t pkv_multi_query_workspace_bytes(int num_seqs) {
+    if (num_seqs < 0) return 0;
+    return round_up(((size_t)num_seqs + 1) * 4, 256);
+}
+
+pkv_status pkv_paged_multi_query_attention(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* query_start, int num_seqs, int total_q,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
+    pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
+    pkv_stream_t stream) {
+    if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+        max_context_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!dtype_bytes(q_dtype) || !dtype_bytes(kv_dtype)) return PKV_ERR_INVALID_ARG;
+    if (!isfinite(scale) || !isfinite(kv_scale) || !(kv_scale > 0.f)) return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if ((q_dtype != PKV_F16 && q_dtype != PKV_BF16) || kv_dtype != q_dtype || head_dim != 128 ||
+        (block_size != 8 && block_size != 16 && block_size != 32) || 128 % group != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    if (!query || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
+        !aligned(query_start, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < pkv_multi_query_workspace_bytes(num_seqs))
+        return PKV_ERR_WORKSPACE;
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    MqParams p{};
+    p.q = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.query_start = query_start;
+    p.out = out;
+    p.item_prefix = static_cast<int*>(workspace);
+    p.status = dev->status;
+    p.num_seqs = num_seqs;
+    p.total_q = total_q;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_context_len = max_context_len;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+    const int64_t items = mq_max_items(num_seqs, total_q, group, num_kv_heads);
+    return cuda_status(launch_mq_attention(p, q_dtype, items,
+                                           static_cast<cudaStream_t>(stream)));
+}
 
 }  // extern "C"

@@ -1,0 +1,460 @@
+// mq_attention.cu -- multi-query causal paged attention on the 5th-generation
+// tensor cores (tcgen05: operands in shared memory, accumulators in TMEM).
+//
+// What it computes ("PagedAttention: Mathematical Foundations, Virtual Memory
+// Block Allocation, and Zero-Waste KV Cache Serving"): §1 -- in the prefill
+// phase a prompt's tokens are processed in parallel as dense tensor-core
+// matrix products, and a token's attention covers every earlier token and
+// itself; §3 -- o = softmax(scale * q K^T) V with K and V gathered block by
+// block through the sequence's table; §7 -- the running max / rescale /
+// running sum of the decode pseudocode, applied here per query row.
+// Query row i of sequence s (query_start[s] + i) is the token at position
+// ctx_s - n_s + i and attends to tokens 0 .. ctx_s - n_s + i.
+//
+// Organisation: one CTA per (sequence, kv head, tile of 128 rows), a row being
+// a (query token, query head of the kv head's group) pair, so the G heads that
+// share a kv head share every K/V tile.  Six warps:
+//   warps 0-3  one thread per row (TMEM lane): Q rows to shared memory, the
+//              softmax of each S tile, the rescale of O, the epilogue;
+//   warp 4     TMA producer: the K and V blocks of each 128-token tile, whole
+//              (block, kv head) rows of the pool, into a 2-stage ring;
+//   warp 5     TMEM allocation; one lane issues the MMAs.
+// Per 128-token tile j:  S_j = Q K_j^T (M 128, N 128, K 128; TMEM, double
+// buffered so S_{j+1} runs while tile j's softmax does), then
+// O += P_j V_j (P from shared memory, V as an MN-major operand; O in TMEM).
+// The running max only moves when a tile's max exceeds it by more than 2^8 (in
+// the log2 domain), and O is rescaled in TMEM only then.
+// Every mbarrier wait is bounded (2 s); on a timeout the CTA flags
+// PKV_DEV_WAIT_TIMEOUT, drains its MMAs and releases its TMEM.
+#include <type_traits>
+
+#include "mq_attention.cuh"
+#include "tcgen05.cuh"
+#include "tmap.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kHD = 128;                              // head dim of this kernel
+constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 B (64 elements)
+constexpr int kTileBytes = 2 * kHalfBytes;            // 128 rows x 256 B
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kTileBytes;                 // 2 stages of (K tile, V tile)
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kOffP = kOffStage + 2 * kStageBytes;
+constexpr int kOffBars = kOffP + kTileBytes;
+constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;                   // S0 [0,128) S1 [128,256) O [256,384)
+constexpr uint32_t kColO = 256;
+constexpr float kMaxSlack = 8.0f;                     // log2-domain headroom before the max moves
+
+static_assert(kOffBars + 256 + 1024 <= 227 * 1024, "shared memory per CTA");
+
+// 16-byte chunk c (0..7) of row r of a 128B-swizzled [rows x 128 B] region.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <typename QT>
+__device__ __forceinline__ uint32_t pack2(float a, float b, float& ra, float& rb) {
+    if constexpr (std::is_same<QT, BF16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        ra = __low2float(h);
+        rb = __high2float(h);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        ra = __low2float(h);
+        rb = __high2float(h);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// Items: per sequence ceil(n * G / 128) row tiles times Hkv; exclusive prefix.
+__global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
+    const int total_q = p.total_q;
+    __shared__ int wsum[32];
+    __shared__ int carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        carry = 0;
+        if (p.query_start[p.num_seqs] != total_q || p.query_start[0] != 0)
+            set_status(p.status, PKV_DEV_BAD_CONTEXT);
+    }
+    const int cap = min(p.max_context_len, p.max_blocks * p.block_size);
+    __syncthreads();
+    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+        const int s = base + tid;
+        int items = 0;
+        if (s < p.num_seqs) {
+            const int n = p.query_start[s + 1] - p.query_start[s];
+            const int ctx = p.context_lens[s];
+            if (n < 0 || ctx < n || ctx > cap || p.query_start[s] < 0 ||
+                p.query_start[s + 1] > total_q) {
+                set_status(p.status, PKV_DEV_BAD_CONTEXT);
+            } else {
+                items = (n * p.group + kMqRows - 1) / kMqRows * p.num_kv_heads;
+            }
+        }
+        int x = items;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int v = wsum[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += y;
+            }
+            wsum[lane] = v;
+        }
+        __syncthreads();
+        const int incl = x + (warp > 0 ? wsum[warp - 1] : 0);
+        if (s < p.num_seqs) p.item_prefix[s] = carry + incl - items;
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry += incl;
+        __syncthreads();
+    }
+    if (tid == 0) p.item_prefix[p.num_seqs] = carry;
+}
+
+template <typename QT>
+__global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
+    MqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sP = smem + kOffP;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint64_t* kv_full = bars;        // [2] TMA bytes of a stage landed
+    uint64_t* kv_empty = bars + 2;   // [2] the stage's last MMA completed
+    uint64_t* s_full = bars + 4;     // [2] S buffer computed
+    uint64_t* q_full = bars + 6;     // Q rows written (128 arrivals)
+    uint64_t* p_full = bars + 7;     // P written, O rescaled (128 arrivals)
+    uint64_t* o_done = bars + 8;     // the tile's P.V completed
+    uint64_t* drain = bars + 9;      // every MMA of the CTA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- this CTA's item: the last sequence whose first item is <= blockIdx.x ----
+    const int b = blockIdx.x;
+    if (b >= p.item_prefix[p.num_seqs]) return;   // whole CTA, before any allocation
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.item_prefix[mid] <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    const int s = lo;
+    const int local = b - p.item_prefix[s];
+    const int G = p.group;
+    const int q_begin = p.query_start[s];
+    const int n = p.query_start[s + 1] - q_begin;
+    const int ctx = p.context_lens[s];
+    const int qpt = kMqRows / G;                          // query tokens per row tile
+    const int tiles = (n * G + kMqRows - 1) / kMqRows;
+    const int qt = tiles - 1 - local / p.num_kv_heads;    // later (longer) tiles first
+    const int kvh = local % p.num_kv_heads;
+    const int q0 = qt * qpt;
+    const int qn = min(qpt, n - q0);
+    const int rows_valid = qn * G;
+    const int pos0 = ctx - n + q0;                        // position of query q0
+    const int kv_end = pos0 + qn;                         // tokens [0, kv_end) are read
+    const int T = (kv_end + kMqTokens - 1) / kMqTokens;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+        }
+        mbar_init(q_full, 128);
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tc5::tmem_alloc(tmem_slot, kTmemCols);
+    tc5::fence_before_sync();
+    __syncthreads();
+    tc5::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ============================ TMA producer ============================
+        if (lane == 0) {
+            prefetch_tensormap(&tmK);
+            prefetch_tensormap(&tmV);
+        }
+        const uint64_t policy = l2_evict_last_policy();   // other row tiles re-read K/V
+        const int B = p.block_size;
+        const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
+        for (int j = 0; j < T; ++j) {
+            const int st = j & 1;
+            if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u)) {
+                set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            const int t0 = j * kMqTokens, t1 = min(t0 + kMqTokens, kv_end);
+            const int fb = t0 / B, nblk = (t1 - 1) / B - fb + 1;   // <= 128 / B <= 16
+            if (lane == 0)
+                mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(nblk * B) * 2u * 256u);
+            __syncwarp();
+            if (lane < nblk) {
+                int phys = trow[fb + lane];
+                if (phys < 0 || phys >= p.num_blocks) {
+                    set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    phys = 0;
+                }
+                const int y = (phys * p.num_kv_heads + kvh) * B;
+                uint8_t* sK = smem + kOffStage + st * kStageBytes + lane * B * 128;
+                uint8_t* sV = sK + kTileBytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_2d(sK + h * kHalfBytes, &tmK, h * 64, y, &kv_full[st], policy);
+                    tma_load_2d(sV + h * kHalfBytes, &tmV, h * 64, y, &kv_full[st], policy);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ============================ MMA issuer =============================
+        if (lane == 0) {
+            constexpr bool kBF16 = std::is_same<QT, BF16>::value;
+            constexpr uint32_t idqk = tc5::idesc_f16(kBF16, 128, 128, false, false);
+            constexpr uint32_t idpv = tc5::idesc_f16(kBF16, 128, 128, false, true);
+            const uint32_t aQ = smem_addr(sQ), aP = smem_addr(sP);
+            bool ok = mbar_wait(q_full, 0);
+            tc5::fence_after_sync();
+            for (int j = 0; j <= T && ok; ++j) {
+                if (j < T) {
+                    // S_j = Q K_j^T into S buffer j % 2 (its previous reader, tile j - 2's
+                    // softmax, finished before P_{j-2} was published)
+                    const int st = j & 1;
+                    if (!mbar_wait(&kv_full[st], (j >> 1) & 1)) { ok = false; break; }
+                    tc5::fence_after_sync();
+                    const uint32_t aK = smem_addr(smem + kOffStage + st * kStageBytes);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
+                        tc5::mma_ss(tmem + (uint32_t)(st * 128),
+                                    tc5::smem_desc_sw128(aQ + off, 16, 1024),
+                                    tc5::smem_desc_sw128(aK + off, 16, 1024), idqk, k > 0);
+                    }
+                    tc5::commit(&s_full[st]);
+                }
+                if (j > 0) {
+                    // O += P_{j-1} V_{j-1}
+                    const int pj = j - 1, st = pj & 1;
+                    if (!mbar_wait(p_full, pj & 1)) { ok = false; break; }
+                    tc5::fence_after_sync();
+                    const uint32_t aV = smem_addr(smem + kOffStage + st * kStageBytes + kTileBytes);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t offp = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
+                        tc5::mma_ss(tmem + kColO, tc5::smem_desc_sw128(aP + offp, 16, 1024),
+                                    tc5::smem_desc_sw128(aV + (uint32_t)(k * 2048), kHalfBytes, 1024),
+                                    idpv, pj > 0 || k > 0);
+                    }
+                    tc5::commit(o_done);
+                    tc5::commit(&kv_empty[st]);
+                }
+            }
+            // every MMA issued above completes before the TMEM is released
+            tc5::commit(drain);
+            if (!mbar_wait(drain, 0)) ok = false;
+            if (!ok) {
+                set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= rows: Q, softmax, O rescale, epilogue =================
+        const int r = threadIdx.x;                        // TMEM lane = row
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int qi = q0 + r / G, hq = kvh * G + r % G;
+        const bool row_valid = r < rows_valid;
+        const int64_t qrow = ((int64_t)(q_begin + qi) * p.num_q_heads + hq) * kHD;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                              (row_valid ? qrow : 0));
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sQ + (c >> 3) * kHalfBytes + sw128(r, c & 7)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(q_full);
+        }
+        const int pos_r = pos0 + r / G;                   // this row's query position
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < T; ++j) {
+            // wait decisions are warp-uniform: the tcgen05 loads and stores below need
+            // the whole warp converged
+            const bool got = !*abort_flag && mbar_wait(&s_full[j & 1], (j >> 1) & 1);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc5::fence_after_sync();
+            uint32_t sv[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+                tc5::ld_32x32b_x32(tmem + lane_base + (uint32_t)((j & 1) * 128 + c4 * 32), sv[c4]);
+            tc5::wait_ld();
+            // local tokens <= lim are visible (rows past the last query see no further)
+            const int lim = min(pos_r, kv_end - 1) - j * kMqTokens;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float x = c4 * 32 + e <= lim ? __uint_as_float(sv[c4][e]) * p.qk_scale_log2
+                                                       : -INFINITY;
+                    sv[c4][e] = __float_as_uint(x);
+                    mx = fmaxf(mx, x);
+                }
+            const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
+            // P and O are free once the previous tile's P.V has completed
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1))) { ok = false; break; }
+                tc5::fence_after_sync();
+            }
+            const bool resc = j > 0 && m_new != m_run;
+            if (__any_sync(0xffffffffu, resc)) {
+                const float f = resc ? fast_exp2(m_run - m_new) : 1.f;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t o[32];
+                    tc5::ld_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                    tc5::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tc5::st_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                }
+                tc5::wait_st();
+                l_run *= f;
+            }
+            m_run = m_new;
+            // P = 2^(x - m) rounded to the operand type; l sums the rounded weights
+            float lsum = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = c8 * 8 + 2 * e;
+                    float ra, rb;
+                    w[e] = pack2<QT>(fast_exp2(__uint_as_float(sv[c >> 5][c & 31]) - m_run),
+                                     fast_exp2(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - m_run),
+                                     ra, rb);
+                    lsum += ra + rb;
+                }
+                *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalfBytes + sw128(r, c8 & 7)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run += lsum;
+            if (j == T - 1 && r >= kv_end - j * kMqTokens) {
+                // V rows past the last token hold poison or stale data: 0 x NaN would
+                // reach O through P = 0
+                uint8_t* vrow = smem + kOffStage + (j & 1) * kStageBytes + kTileBytes + r * 128;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(vrow + h * kHalfBytes + c * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            tc5::fence_before_sync();
+            mbar_arrive(p_full);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(o_done, (T - 1) & 1));
+        if (ok) {
+            tc5::fence_after_sync();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t o[32];
+                tc5::ld_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                tc5::wait_ld();
+                if (row_valid) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float ra, rb;
+                        w[e] = pack2<QT>(__uint_as_float(o[2 * e]) * inv,
+                                         __uint_as_float(o[2 * e + 1]) * inv, ra, rb);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow +
+                                                          c4 * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+            }
+        } else {
+            set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc5::fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc5::fence_after_sync();
+        tc5::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <typename QT>
+cudaError_t launch_typed(const MqParams& p, int64_t max_items, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    auto kernel = mq_attention_kernel<QT>;
+    if (!attr_set[dev]) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (err != cudaSuccess) return err;
+        attr_set[dev] = true;
+    }
+    CUtensorMap tk, tv;
+    const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    if (!encode_pool_map(&tk, p.k_cache, kHD, 2, rows, p.block_size) ||
+        !encode_pool_map(&tv, p.v_cache, kHD, 2, rows, p.block_size))
+        return cudaErrorInvalidValue;
+    mq_plan_kernel<<<1, 1024, 0, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    kernel<<<(unsigned)max_items, kThreads, kSmem, stream>>>(p, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int64_t mq_max_items(int num_seqs, int total_q, int group, int num_kv_heads) {
+    return (int64_t)num_kv_heads * (((int64_t)total_q * group + kMqRows - 1) / kMqRows + num_seqs);
+}
+
+cudaError_t launch_mq_attention(const MqParams& p, pkv_dtype q_dtype, int64_t max_items,
+                                cudaStream_t stream) {
+    if (max_items <= 0) return cudaSuccess;
+    if (max_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    switch (q_dtype) {
+    case PKV_F16: return launch_typed<F16>(p, max_items, stream);
+    case PKV_BF16: return launch_typed<BF16>(p, max_items, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,35 @@
+// mq_attention.cuh -- parameters and launcher of the multi-query (causal) paged
+// attention: several query tokens per sequence over the paged KV cache, for
+// prefill, chunked prefill and the verification of a chain of draft tokens.
+#pragma once
+
+#include "common.cuh"
+
+namespace pkv {
+
+constexpr int kMqRows = 128;     // (query token, head of the group) rows per CTA tile
+constexpr int kMqTokens = 128;   // K/V tokens per pipeline tile
+
+struct MqParams {
+    const void* q;                 // [total_q, Hq, d]
+    const void* k_cache;           // [NB, Hkv, B, d]
+    const void* v_cache;
+    const int32_t* block_tables;   // [S, max_blocks]
+    const int32_t* context_lens;   // [S]: tokens in the cache, the queries' own included
+    const int32_t* query_start;    // [S + 1]: query rows of sequence s
+    void* out;                     // [total_q, Hq, d]
+    int* item_prefix;              // workspace [S + 1]: (seq, kv head, row tile) items
+    unsigned* status;
+    int num_seqs, total_q, num_q_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
+    int max_blocks;
+    int max_context_len;
+    float qk_scale_log2;           // scale * log2(e)
+};
+
+// Upper bound of the CTAs the launch needs (items of every sequence).
+int64_t mq_max_items(int num_seqs, int total_q, int group, int num_kv_heads);
+
+cudaError_t launch_mq_attention(const MqParams& p, pkv_dtype q_dtype, int64_t max_items,
+                                cudaStream_t stream);
+
+}  // namespace pkv

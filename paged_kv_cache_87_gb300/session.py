@@ -9,7 +9,7 @@ import numpy as np
 import torch
 
 from . import binding
-from .inputs import Workload
+from .inputs import MultiQueryWorkload, Workload
 
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
                "e4m3": torch.float8_e4m3fn}
@@ -108,6 +108,60 @@ class DeviceState:
         self.copy_step(stream)
         self.append_step(stream)
         return self.decode(stream)
+
+    def out_f64(self) -> np.ndarray:
+        return self.out.detach().to(torch.float64).cpu().numpy()
+
+
+class MultiQueryState:
+    """A multi-query workload's pool, tables and queries resident on one CUDA device.
+
+    ``run_setup`` writes the tokens cached before the step; ``step`` writes the
+    queries' own K/V rows and runs the multi-query attention.
+    """
+
+    def __init__(self, w: MultiQueryWorkload, device="cuda"):
+        self.w = w
+        dev = self.device = torch.device(device)
+        self.k_cache = poisoned_cache(w.cache_shape, w.kv_dtype, dev)
+        self.v_cache = poisoned_cache(w.cache_shape, w.kv_dtype, dev)
+        self.query = host_tensor(w.query, w.q_dtype).to(dev)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.context_lens = torch.from_numpy(w.context_lens).to(dev)
+        self.query_start = torch.from_numpy(w.query_start).to(dev)
+        self.new_key = host_tensor(w.key[w.new_idx], w.kv_dtype).to(dev)
+        self.new_value = host_tensor(w.value[w.new_idx], w.kv_dtype).to(dev)
+        self.new_slots = torch.from_numpy(np.ascontiguousarray(w.slots[w.new_idx])).to(dev)
+        self.out = torch.empty_like(self.query)
+        self.workspace = torch.empty(max(256, binding.pkv_multi_query_workspace_bytes(w.num_seqs)),
+                                     dtype=torch.uint8, device=dev)
+
+    def run_setup(self, chunk_tokens: int = 1 << 20) -> None:
+        w = self.w
+        idx = w.prior_idx
+        for a in range(0, len(idx), chunk_tokens):
+            sl = idx[a:a + chunk_tokens]
+            k = host_tensor(w.key[sl], w.kv_dtype).to(self.device)
+            v = host_tensor(w.value[sl], w.kv_dtype).to(self.device)
+            s = torch.from_numpy(np.ascontiguousarray(w.slots[sl])).to(self.device)
+            binding.pkv_reshape_and_cache(k, v, self.k_cache, self.v_cache, s)
+        torch.cuda.synchronize(self.device)
+
+    def append_step(self, stream=None) -> None:
+        binding.pkv_reshape_and_cache(self.new_key, self.new_value, self.k_cache, self.v_cache,
+                                      self.new_slots, stream=stream)
+
+    def attend(self, stream=None, out=None) -> torch.Tensor:
+        w = self.w
+        return binding.pkv_paged_multi_query_attention(
+            self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+            self.query_start, w.max_context_len, w.scale, workspace=self.workspace,
+            out=self.out if out is None else out, stream=stream)
+
+    def step(self, stream=None) -> torch.Tensor:
+        """One pass: write the queries' own K/V, then attend."""
+        self.append_step(stream)
+        return self.attend(stream)
 
     def out_f64(self) -> np.ndarray:
         return self.out.detach().to(torch.float64).cpu().numpy()

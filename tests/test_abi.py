@@ -88,6 +88,38 @@ def test_decode_host_validation(lib):
     assert _decode(lib, S=0, query=None, k=None) == E.PKV_OK       # nothing to do
 
 
+def _multi_query(lib, **kw):
+    a = dict(query=1024, k=1024, v=1024, bt=1024, cl=1024, qs=1024, S=4, tq=16, Hq=8, Hkv=2,
+             d=128, B=16, NB=64, mb=16, mctx=256, scale=0.088, qt=2, kt=2, kvs=1.0, ws=None,
+             wsb=0, out=1024)
+    a.update(kw)
+    return lib.pkv_paged_multi_query_attention(
+        a["query"], a["k"], a["v"], a["bt"], a["cl"], a["qs"], a["S"], a["tq"], a["Hq"],
+        a["Hkv"], a["d"], a["B"], a["NB"], a["mb"], a["mctx"], a["scale"], a["qt"], a["kt"],
+        a["kvs"], a["ws"], a["wsb"], a["out"], None)
+
+
+def test_multi_query_host_validation(lib):
+    E = binding
+    assert _multi_query(lib, query=None) == E.PKV_ERR_INVALID_ARG
+    assert _multi_query(lib, qs=None) == E.PKV_ERR_INVALID_ARG
+    assert _multi_query(lib, qt=0, kt=0) == E.PKV_ERR_UNSUPPORTED   # fp32
+    assert _multi_query(lib, kt=3) == E.PKV_ERR_UNSUPPORTED          # FP8 K/V
+    assert _multi_query(lib, qt=1) == E.PKV_ERR_UNSUPPORTED          # f16 q, bf16 cache
+    assert _multi_query(lib, d=64) == E.PKV_ERR_UNSUPPORTED
+    assert _multi_query(lib, B=12) == E.PKV_ERR_UNSUPPORTED
+    assert _multi_query(lib, Hq=6) == E.PKV_ERR_UNSUPPORTED          # group 3 does not divide 128
+    assert _multi_query(lib, Hkv=3) == E.PKV_ERR_INVALID_ARG
+    assert _multi_query(lib, kvs=0.0) == E.PKV_ERR_INVALID_ARG
+    assert _multi_query(lib, mctx=16 * 16 + 1) == E.PKV_ERR_INVALID_ARG
+    assert _multi_query(lib, qs=1024 + 2) == E.PKV_ERR_INVALID_ARG   # misaligned
+    assert _multi_query(lib) == E.PKV_ERR_WORKSPACE
+    assert _multi_query(lib, ws=4096, wsb=8) == E.PKV_ERR_WORKSPACE
+    assert _multi_query(lib, tq=0, query=None) == E.PKV_OK           # nothing to do
+    assert binding.pkv_multi_query_workspace_bytes(4) == 256
+    assert binding.pkv_multi_query_workspace_bytes(1000) == 4096
+
+
 def test_reshape_and_copy_host_validation(lib):
     E = binding
     f = lib.pkv_reshape_and_cache

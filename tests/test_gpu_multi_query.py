@@ -1,0 +1,194 @@
+"""Multi-query (causal) paged attention on the GPU against the oracle.
+
+Query row i of a sequence with n queries and ctx cached tokens attends to tokens
+0 .. ctx - n + i ("PagedAttention: Mathematical Foundations ..." §1 prefill,
+§3 attention through the block table).  The kernel runs Q K^T and P V on the
+tcgen05 tensor cores; P is rounded to the operand type, so the comparison is by
+the dtype's tolerance.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_87_gb300 import binding, inputs
+from paged_kv_cache_87_gb300.session import MultiQueryState
+from tests.helpers import TOL
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_pool(w):
+    kc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+    vc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+    oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slots, num_kv_heads=w.num_kv_heads,
+                             head_dim=w.head_dim, block_size=w.block_size,
+                             num_blocks=w.num_blocks, src_dtype=w.kv_dtype,
+                             kv_dtype=w.kv_dtype)
+    return kc, vc
+
+
+def _oracle(w, sel=None):
+    kc, vc = _oracle_pool(w)
+    return oracle.paged_prefill_attention(
+        w.query, kc, vc, w.block_tables, w.context_lens, w.query_start,
+        num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+        block_size=w.block_size, num_blocks=w.num_blocks, scale=w.scale, q_dtype=w.q_dtype,
+        kv_dtype=w.kv_dtype, sel=sel, nthreads=8)
+
+
+def _gpu(w):
+    st = MultiQueryState(w)
+    st.run_setup()
+    binding.pkv_get_device_status()          # clear
+    st.step()
+    torch.cuda.synchronize()
+    return st
+
+
+def _check(w):
+    st = _gpu(w)
+    got = st.out_f64()
+    ref = _oracle(w)
+    assert binding.pkv_get_device_status() == 0
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= TOL[w.q_dtype], err
+    return st
+
+
+def test_mixed_query_counts_bf16():
+    _check(inputs.make_multi_query_config(0))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (8, 2), (16, 2), (16, 1)])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_groups_dtypes_block_sizes(dt, Hq, Hkv, B):
+    rng = np.random.default_rng(Hq * 1000 + Hkv * 100 + B)
+    w = inputs.make_multi_query("mq", rng, [0, 70, 250], [1, 40, 150], num_q_heads=Hq,
+                                num_kv_heads=Hkv, head_dim=128, block_size=B, dtype=dt)
+    _check(w)
+
+
+def test_prompts_without_prior_context_ragged_tiles():
+    rng = np.random.default_rng(21)
+    w = inputs.make_multi_query("prefill", rng, [0, 0, 0], [129, 300, 1], num_q_heads=4,
+                                num_kv_heads=4, head_dim=128, block_size=16, dtype="bf16")
+    _check(w)
+
+
+def test_long_prior_context_many_kv_tiles():
+    rng = np.random.default_rng(22)
+    w = inputs.make_multi_query("long", rng, [3000, 1700], [200, 70], num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, block_size=16, dtype="bf16")
+    _check(w)
+
+
+def test_scaled_logits_move_the_running_max():
+    """Large logits (scale 0.35 instead of 1/sqrt(128)) make later tiles exceed the
+    running max by more than the rescale headroom, exercising the O rescale in
+    tensor memory."""
+    rng = np.random.default_rng(23)
+    w = inputs.make_multi_query("big logits", rng, [900], [100], num_q_heads=4, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="bf16", scale=0.35)
+    _check(w)
+
+
+def test_physical_block_relabelling_is_bit_invariant():
+    rng = np.random.default_rng(24)
+    w = inputs.make_multi_query("relabel", rng, [100, 333], [60, 90], num_q_heads=8,
+                                num_kv_heads=2, head_dim=128, block_size=16, dtype="bf16")
+    a = _gpu(w).out.clone()
+    perm = np.random.default_rng(5).permutation(w.num_blocks)
+    w2 = inputs.MultiQueryWorkload(**{**w.__dict__, "slots": perm[w.slots // w.block_size] *
+                                      w.block_size + w.slots % w.block_size,
+                                      "block_tables": np.where(w.block_tables >= 0,
+                                                               perm[np.maximum(w.block_tables, 0)],
+                                                               -1).astype(np.int32)})
+    b = _gpu(w2).out
+    assert torch.equal(a, b)
+
+
+def test_one_query_per_sequence_equals_the_decode_kernel():
+    rng = np.random.default_rng(25)
+    w = inputs.make_multi_query("one", rng, [10, 500, 2047, 64], [1, 1, 1, 1], num_q_heads=16,
+                                num_kv_heads=4, head_dim=128, block_size=16, dtype="bf16")
+    st = _gpu(w)
+    dec = binding.pkv_paged_decode_attention(st.query, st.k_cache, st.v_cache, st.block_tables,
+                                             st.context_lens, w.max_context_len, w.scale)
+    torch.cuda.synchronize()
+    err = (st.out.double() - dec.double()).abs().max().item()
+    assert err <= TOL["bf16"], err
+    ref = _oracle(w)
+    assert np.abs(st.out_f64() - ref).max() <= TOL["bf16"]
+
+
+def test_sequence_with_more_queries_than_context_is_flagged_and_skipped():
+    rng = np.random.default_rng(26)
+    w = inputs.make_multi_query("bad", rng, [20, 40], [10, 10], num_q_heads=4, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="bf16")
+    st = MultiQueryState(w)
+    st.run_setup()
+    st.append_step()
+    st.context_lens[0] = 5                   # 10 queries over 5 tokens: a contract violation
+    st.out.fill_(7.0)
+    binding.pkv_get_device_status()
+    st.attend()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_CONTEXT
+    assert torch.all(st.out[:10] == 7.0)     # the bad sequence's rows are untouched
+    ref = _oracle(w)
+    assert np.abs(st.out_f64()[10:] - ref[10:]).max() <= TOL["bf16"]
+
+
+def test_unsupported_shapes_and_types_are_refused():
+    rng = np.random.default_rng(27)
+    w = inputs.make_multi_query("f32", rng, [5], [3], num_q_heads=2, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="f32")
+    st = MultiQueryState(w)
+    with pytest.raises(binding.PagedKVError) as e:
+        st.attend()
+    assert e.value.status == binding.PKV_ERR_UNSUPPORTED
+    w = inputs.make_multi_query("d64", rng, [5], [3], num_q_heads=2, num_kv_heads=2,
+                                head_dim=64, block_size=16, dtype="bf16")
+    st = MultiQueryState(w)
+    with pytest.raises(binding.PagedKVError) as e:
+        st.attend()
+    assert e.value.status == binding.PKV_ERR_UNSUPPORTED
+    w = inputs.make_multi_query("g3", rng, [5], [3], num_q_heads=6, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="bf16")
+    st = MultiQueryState(w)
+    with pytest.raises(binding.PagedKVError) as e:
+        st.attend()
+    assert e.value.status == binding.PKV_ERR_UNSUPPORTED
+
+
+def test_no_queries_is_a_no_op():
+    rng = np.random.default_rng(28)
+    w = inputs.make_multi_query("empty", rng, [5, 9], [0, 0], num_q_heads=2, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="bf16")
+    st = MultiQueryState(w)
+    st.attend()
+    torch.cuda.synchronize()
+
+
+def test_chunked_prefill_workload_sampled():
+    """The benchmark's workload at full size: sampled rows of every sequence."""
+    w = inputs.make_multi_query_config(1)
+    st = _gpu(w)
+    assert binding.pkv_get_device_status() == 0
+    got = st.out_f64()
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(0)
+    rows = []
+    for s in range(w.num_seqs):
+        q0, q1 = int(w.query_start[s]), int(w.query_start[s + 1])
+        rows += [q0, q1 - 1] + list(rng.integers(q0, q1, size=2))
+    sel = np.array([(r, int(h)) for r in rows for h in rng.integers(0, w.num_q_heads, size=2)],
+                   dtype=np.int32)
+    ref = _oracle(w, sel=sel)
+    err = np.abs(got[sel[:, 0], sel[:, 1]] - ref).max()
+    assert err <= TOL["bf16"], err
