@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak); µs per decode step"
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ["common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh",
                   "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "tmap.cu", "tmap.cuh",
@@ -53,6 +54,9 @@ def parse_args(argv=None):
                     help="measure pkv_swap_blocks (device pool <-> pinned host pool) instead")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--multi-query", type=int, default=None, metavar="ID",
+                    help="measure the multi-query (causal) paged attention on multi-query "
+                         "workload ID (1: chunked prefill) instead of the decode")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="store the DRAM bytes per decode launch of an ncu --csv capture "
                          "(dram__bytes_read.sum, dram__bytes_write.sum of decode_mma / "
@@ -210,7 +214,7 @@ def decode_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: int):
+def recorded_traffic(workload):
     """DRAM bytes per decode launch from a committed ncu summary, if it matches this code."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(path):
@@ -223,7 +227,8 @@ def recorded_traffic(workload: int):
     return rec.get("dram_bytes_per_launch")
 
 
-def record_traffic(csv_path: str, workload: int) -> dict:
+def record_traffic(csv_path: str, workload, kernels=("decode_mma_kernel",
+                                                      "decode_simt_kernel")) -> dict:
     """Average DRAM bytes (read + write) per decode launch of an ncu --csv log,
     stored for `workload` with the hash of the decode sources it was taken on."""
     import csv
@@ -235,13 +240,13 @@ def record_traffic(csv_path: str, workload: int) -> dict:
              "KB": 1e3, "MB": 1e6, "GB": 1e9}
     per = {}
     for r in rows[1:]:
-        if "decode_mma_kernel" not in r[ki] and "decode_simt_kernel" not in r[ki]:
+        if not any(k in r[ki] for k in kernels):
             continue
         if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             per.setdefault(r[ii], 0.0)
             per[r[ii]] += float(r[vi].replace(",", "")) * scale[r[ui]]
     if not per:
-        raise SystemExit(f"no decode launch with DRAM byte counters in {csv_path}")
+        raise SystemExit(f"no {'/'.join(kernels)} launch with DRAM byte counters in {csv_path}")
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     d = json.load(open(path)) if os.path.exists(path) else {}
     d[str(workload)] = {"dram_bytes_per_launch": sum(per.values()) / len(per),
@@ -430,6 +435,198 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+MQ_METRIC = "multi-query causal paged attention: TFLOP/s (of measured bf16 dense peak)"
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json, bf16 burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def mq_oracle_sample(w, target_s: float, nthreads: int, seed: int = 0, caches=None):
+    """The oracle on sampled (query row, head) pairs; returns (TFLOP/s, s, flops, desc)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    if caches is None:
+        from paged_kv_cache_87_gb300 import inputs
+        kc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+        vc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+        oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slots, num_kv_heads=w.num_kv_heads,
+                                 head_dim=w.head_dim, block_size=w.block_size,
+                                 num_blocks=w.num_blocks, src_dtype=w.kv_dtype,
+                                 kv_dtype=w.kv_dtype)
+    else:
+        kc, vc = caches
+    seq_of_row = np.repeat(np.arange(w.num_seqs), np.diff(w.query_start))
+    pos = (w.context_lens[seq_of_row] - np.diff(w.query_start)[seq_of_row] +
+           (np.arange(w.total_q) - w.query_start[seq_of_row]))
+
+    def run(k):
+        rows = rng.integers(0, w.total_q, size=k)
+        heads = rng.integers(0, w.num_q_heads, size=k)
+        sel = np.stack([rows, heads], 1).astype(np.int32)
+        t = time.perf_counter()
+        oracle.paged_prefill_attention(
+            w.query, kc, vc, w.block_tables, w.context_lens, w.query_start,
+            num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+            block_size=w.block_size, num_blocks=w.num_blocks, scale=w.scale, q_dtype=w.q_dtype,
+            kv_dtype=w.kv_dtype, sel=sel, nthreads=nthreads)
+        dt = time.perf_counter() - t
+        return dt, int(4 * w.head_dim * (pos[rows] + 1).sum())
+
+    dt, fl = run(max(8, nthreads))                         # calibration
+    k = int(max(8, nthreads) * max(1.0, target_s / max(dt, 1e-3)))
+    dt, fl = run(k)
+    return fl / dt / 1e12, dt, fl, (f"{k} random (query row, head) pairs of the workload, "
+                                    f"{nthreads} threads")
+
+
+def run_mq(args, rank, world, local):
+    """The multi-query workload: per step, write the queries' own K/V and attend."""
+    import torch
+    from paged_kv_cache_87_gb300 import binding, build, inputs
+    from paged_kv_cache_87_gb300.session import MultiQueryState, host_tensor
+
+    build.build()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    w = inputs.make_multi_query_config(args.multi_query)
+    st = MultiQueryState(w, device)
+    st.run_setup()
+    stream = torch.cuda.Stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(2 * l2 // 4 * 4, dtype=torch.uint8, device=device)
+    launches_per_step = 3                     # reshape_and_cache, plan, attention
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            st.step(stream)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(device)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_buf.zero_()
+            s0, a0, a1, s1 = ev[i]
+            s0.record(stream)
+            st.append_step(stream)
+            a0.record(stream)
+            st.attend(stream)
+            a1.record(stream)
+            s1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(world)
+    clk = clocks.stop()
+    assert binding.pkv_get_device_status() == 0, "device status flagged during the benchmark"
+    sec_step = float(np.mean([e[0].elapsed_time(e[3]) for e in ev])) * 1e-3
+    sec_att = float(np.mean([e[1].elapsed_time(e[2]) for e in ev])) * 1e-3
+    total, slowest, _ = aggregate(w.flops, sec_step, world, device)
+    value = total / slowest / 1e12
+
+    # end to end: the step's inputs from pinned host memory, the output back, every step
+    pin = lambda t: t.pin_memory()
+    ins = [(pin(host_tensor(w.query, w.q_dtype)), st.query),
+           (pin(host_tensor(w.key[w.new_idx], w.kv_dtype)), st.new_key),
+           (pin(host_tensor(w.value[w.new_idx], w.kv_dtype)), st.new_value),
+           (pin(torch.from_numpy(np.ascontiguousarray(w.slots[w.new_idx]))), st.new_slots),
+           (pin(torch.from_numpy(w.context_lens)), st.context_lens),
+           (pin(torch.from_numpy(w.query_start)), st.query_start),
+           (pin(torch.from_numpy(w.block_tables)), st.block_tables)]
+    h_out = pin(torch.empty_like(st.out, device="cpu"))
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush_buf.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for h, d in ins:
+                d.copy_(h, non_blocking=True)
+            st.step(stream)
+            h_out.copy_(st.out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    tot_e, slow_e, _ = aggregate(w.flops, float(np.mean(e2e_ms)) * 1e-3, world, device)
+
+    peak, peak_src = measured_tensor_peak()
+    achieved = w.flops / sec_att / 1e12
+    traffic = recorded_traffic(f"mq{args.multi_query}")
+    line = {
+        "metric": MQ_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(slowest * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.q_dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V; seeded block permutation)",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "total_queries": w.total_q,
+                   "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "block_size": w.block_size,
+                   "flops_per_step": w.flops, "kv_bytes": w.kv_bytes,
+                   "l2": "L2 flushed between steps (write of 2x L2)",
+                   "step": "reshape_and_cache of the queries' tokens + multi-query attention",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "planning + attention kernels (CUDA events around the call)",
+                     "attention_us": round(sec_att * 1e6, 2)},
+        "e2e": {"value": round(tot_e / slow_e / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(float(np.mean(e2e_ms)), 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, fl, desc = mq_oracle_sample(w, args.cpu_seconds, os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s",
+                                "cores": os.cpu_count() or 1, "kind": "oracle", "sample": desc,
+                                "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_mq_reference(args, rank, world, local):
+    """The oracle on host cores, each step a bounded sample of the multi-query workload."""
+    if rank != 0:
+        return
+    from paged_kv_cache_87_gb300 import inputs
+    import oracle
+    oracle.build()
+    w = inputs.make_multi_query_config(args.multi_query)
+    kc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+    vc = inputs.poison_array(w.cache_shape, w.kv_dtype)
+    oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slots, num_kv_heads=w.num_kv_heads,
+                             head_dim=w.head_dim, block_size=w.block_size,
+                             num_blocks=w.num_blocks, src_dtype=w.kv_dtype, kv_dtype=w.kv_dtype)
+    threads = os.cpu_count() or 1
+    per = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    res = []
+    for i in range(args.warmup + args.steps):
+        v, secs, fl, desc = mq_oracle_sample(w, per, threads, seed=i, caches=(kc, vc))
+        if i >= args.warmup:
+            res.append((v, secs, fl))
+    value = sum(r[2] for r in res) / sum(r[1] for r in res) / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": MQ_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(float(np.mean([r[1] for r in res])) * 1e3, 3),
+        "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
 def run_reference(args, rank, world, local):
     """The oracle, as it stands, on host cores: each step a bounded sample of the workload."""
     if rank != 0:
@@ -511,7 +708,17 @@ def main(argv=None):
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.record_traffic:
-        print(json.dumps(record_traffic(args.record_traffic, args.workload)))
+        if args.multi_query is not None:
+            rec = record_traffic(args.record_traffic, f"mq{args.multi_query}",
+                                 kernels=("mq_attention_kernel",))
+        else:
+            rec = record_traffic(args.record_traffic, args.workload)
+        print(json.dumps(rec))
+    elif args.multi_query is not None:
+        if args.impl == "reference":
+            run_mq_reference(args, rank, world, local)
+        else:
+            run_mq(args, rank, world, local)
     elif args.swap:
         run_swap(args, rank, world, local)
     elif args.impl == "reference":

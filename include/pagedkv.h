@@ -195,7 +195,7 @@ PKV_API pkv_status pkv_paged_decode_attention_prefix(
  * head_dim 128, block_size in {8, 16, 32}, num_q_heads / num_kv_heads a
  * divisor of 128; others return PKV_ERR_UNSUPPORTED.  Q K^T and P V run on the
  * tcgen05 tensor cores with fp32 accumulation in tensor memory; P is rounded
- * to q_dtype before P V (the softmax denominator sums the rounded weights).
+ * to q_dtype before P V (the softmax denominator sums the fp32 weights).
  * Two launches on `stream`: a one-CTA planning kernel and the attention
  * kernel (one CTA per sequence, kv head and 128 (query, head) rows).
  */

@@ -39,12 +39,14 @@ constexpr int kHD = 128;                              // head dim of this kernel
 constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 B (64 elements)
 constexpr int kTileBytes = 2 * kHalfBytes;            // 128 rows x 256 B
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kTileBytes;                 // 2 stages of (K tile, V tile)
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kOffP = kOffStage + 2 * kStageBytes;
+constexpr int kKStages = 3;                           // K ring: freed when S_j completes
+constexpr int kVStages = 2;                           // V ring: freed when P_j V_j completes
+constexpr int kOffK = kTileBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;
 constexpr int kOffBars = kOffP + kTileBytes;
 constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                         // 4 row warps, K and V producers, MMA
 constexpr uint32_t kTmemCols = 512;                   // S0 [0,128) S1 [128,256) O [256,384)
 constexpr uint32_t kColO = 256;
 constexpr float kMaxSlack = 8.0f;                     // log2-domain headroom before the max moves
@@ -67,6 +69,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, float& ra, float& rb
         const __half2 h = __floats2half2_rn(a, b);
         ra = __low2float(h);
         rb = __high2float(h);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+template <typename QT>
+__device__ __forceinline__ uint32_t pack2_bits(float a, float b) {
+    if constexpr (std::is_same<QT, BF16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
         return *reinterpret_cast<const uint32_t*>(&h);
     }
 }
@@ -133,14 +146,16 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sP = smem + kOffP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    uint64_t* kv_full = bars;        // [2] TMA bytes of a stage landed
-    uint64_t* kv_empty = bars + 2;   // [2] the stage's last MMA completed
-    uint64_t* s_full = bars + 4;     // [2] S buffer computed
-    uint64_t* q_full = bars + 6;     // Q rows written (128 arrivals)
-    uint64_t* p_full = bars + 7;     // P written, O rescaled (128 arrivals)
-    uint64_t* o_done = bars + 8;     // the tile's P.V completed
-    uint64_t* drain = bars + 9;      // every MMA of the CTA completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+    uint64_t* k_full = bars;         // [3] TMA bytes of a K stage landed
+    uint64_t* k_empty = bars + 3;    // [3] the S MMA reading the K stage completed
+    uint64_t* v_full = bars + 6;     // [2] TMA bytes of a V stage landed
+    uint64_t* v_empty = bars + 8;    // [2] the P.V MMA reading the V stage completed
+    uint64_t* s_full = bars + 10;    // [2] S buffer computed
+    uint64_t* q_full = bars + 12;    // Q rows written (128 arrivals)
+    uint64_t* p_full = bars + 13;    // P written, O rescaled (128 arrivals)
+    uint64_t* o_done = bars + 14;    // the tile's P.V completed
+    uint64_t* drain = bars + 15;     // every MMA of the CTA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,11 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     const int T = (kv_end + kMqTokens - 1) / kMqTokens;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
-            mbar_init(&s_full[i], 1);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
         }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
         mbar_init(q_full, 128);
         mbar_init(p_full, 128);
         mbar_init(o_done, 1);
@@ -190,41 +209,39 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     tc5::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ============================ TMA producer ============================
-        if (lane == 0) {
-            prefetch_tensormap(&tmK);
-            prefetch_tensormap(&tmV);
-        }
+    if (warp == 4 || warp == 6) {
+        // ===================== TMA producers: warp 4 K, warp 6 V =====================
+        const bool isK = warp == 4;
+        const CUtensorMap* map = isK ? &tmK : &tmV;
+        if (lane == 0) prefetch_tensormap(map);
         const uint64_t policy = l2_evict_last_policy();   // other row tiles re-read K/V
         const int B = p.block_size;
+        const int nst = isK ? kKStages : kVStages;
+        uint64_t* full = isK ? k_full : v_full;
+        uint64_t* empty = isK ? k_empty : v_empty;
+        uint8_t* ring = smem + (isK ? kOffK : kOffV);
         const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
         for (int j = 0; j < T; ++j) {
-            const int st = j & 1;
-            if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u)) {
+            const int st = j % nst;
+            if (!mbar_wait(&empty[st], ((j / nst) & 1) ^ 1u)) {
                 set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
                 *abort_flag = 1;
                 break;
             }
             const int t0 = j * kMqTokens, t1 = min(t0 + kMqTokens, kv_end);
             const int fb = t0 / B, nblk = (t1 - 1) / B - fb + 1;   // <= 128 / B <= 16
-            if (lane == 0)
-                mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(nblk * B) * 2u * 256u);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nblk * B) * 256u);
             __syncwarp();
             if (lane < nblk) {
                 int phys = trow[fb + lane];
                 if (phys < 0 || phys >= p.num_blocks) {
-                    set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    if (isK) set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
                     phys = 0;
                 }
                 const int y = (phys * p.num_kv_heads + kvh) * B;
-                uint8_t* sK = smem + kOffStage + st * kStageBytes + lane * B * 128;
-                uint8_t* sV = sK + kTileBytes;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tma_load_2d(sK + h * kHalfBytes, &tmK, h * 64, y, &kv_full[st], policy);
-                    tma_load_2d(sV + h * kHalfBytes, &tmV, h * 64, y, &kv_full[st], policy);
-                }
+                uint8_t* dst = ring + st * kTileBytes + lane * B * 128;
+                tma_load_2d(dst, map, 0, y, &full[st], policy);
+                tma_load_2d(dst + kHalfBytes, map, 64, y, &full[st], policy);
             }
         }
     } else if (warp == 5) {
@@ -240,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 if (j < T) {
                     // S_j = Q K_j^T into S buffer j % 2 (its previous reader, tile j - 2's
                     // softmax, finished before P_{j-2} was published)
-                    const int st = j & 1;
-                    if (!mbar_wait(&kv_full[st], (j >> 1) & 1)) { ok = false; break; }
+                    const int st = j & 1, ks = j % kKStages;
+                    if (!mbar_wait(&k_full[ks], (j / kKStages) & 1)) { ok = false; break; }
                     tc5::fence_after_sync();
-                    const uint32_t aK = smem_addr(smem + kOffStage + st * kStageBytes);
+                    const uint32_t aK = smem_addr(smem + kOffK + ks * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t off = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
@@ -252,13 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                                     tc5::smem_desc_sw128(aK + off, 16, 1024), idqk, k > 0);
                     }
                     tc5::commit(&s_full[st]);
+                    tc5::commit(&k_empty[ks]);
                 }
                 if (j > 0) {
                     // O += P_{j-1} V_{j-1}
-                    const int pj = j - 1, st = pj & 1;
-                    if (!mbar_wait(p_full, pj & 1)) { ok = false; break; }
+                    const int pj = j - 1, vs = pj % kVStages;
+                    if (!mbar_wait(p_full, pj & 1) ||
+                        !mbar_wait(&v_full[vs], (pj / kVStages) & 1)) { ok = false; break; }
                     tc5::fence_after_sync();
-                    const uint32_t aV = smem_addr(smem + kOffStage + st * kStageBytes + kTileBytes);
+                    const uint32_t aV = smem_addr(smem + kOffV + vs * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t offp = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                                     idpv, pj > 0 || k > 0);
                     }
                     tc5::commit(o_done);
-                    tc5::commit(&kv_empty[st]);
+                    tc5::commit(&v_empty[vs]);
                 }
             }
             // every MMA issued above completes before the TMEM is released
@@ -313,16 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             tc5::wait_ld();
             // local tokens <= lim are visible (rows past the last query see no further)
             const int lim = min(pos_r, kv_end - 1) - j * kMqTokens;
-            float mx = -INFINITY;
+            // a tile every row of the warp sees whole needs no mask
+            if (!__all_sync(0xffffffffu, lim >= kMqTokens - 1)) {
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
+                for (int c = 0; c < kMqTokens; ++c)
+                    if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+            }
+            // row max of the raw scores (the scale is positive: same order), with 8
+            // independent partial maxima instead of one 128-long chain
+            float pmx[8];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = c4 * 32 + e <= lim ? __uint_as_float(sv[c4][e]) * p.qk_scale_log2
-                                                       : -INFINITY;
-                    sv[c4][e] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
-                }
+            for (int i = 0; i < 8; ++i) pmx[i] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kMqTokens; ++c)
+                pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(sv[c >> 5][c & 31]));
+#pragma unroll
+            for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
+            const float mx = pmx[0] * p.qk_scale_log2;
             const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
             // P and O are free once the previous tile's P.V has completed
             if (j > 0) {
@@ -345,28 +371,44 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 l_run *= f;
             }
             m_run = m_new;
-            // P = 2^(x - m) rounded to the operand type; l sums the rounded weights
-            float lsum = 0.f;
+            // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
+            // operand type; l sums the weights, 8 partial sums
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+            float pls[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pls[i] = 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < 16; ++c8) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = c8 * 8 + 2 * e;
-                    float ra, rb;
-                    w[e] = pack2<QT>(fast_exp2(__uint_as_float(sv[c >> 5][c & 31]) - m_run),
-                                     fast_exp2(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]) - m_run),
-                                     ra, rb);
-                    lsum += ra + rb;
+                    const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
+                                                   p.qk_scale_log2, neg_m));
+                    const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
+                                                    p.qk_scale_log2, neg_m));
+                    w[e] = pack2_bits<QT>(a, bb);
+                    pls[(2 * e) & 7] += a;
+                    pls[(2 * e + 1) & 7] += bb;
                 }
                 *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalfBytes + sw128(r, c8 & 7)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
+            float lsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) lsum += pls[i];
             l_run += lsum;
-            if (j == T - 1 && r >= kv_end - j * kMqTokens) {
+            if (j == T - 1 && kv_end - j * kMqTokens < kMqTokens) {
                 // V rows past the last token hold poison or stale data: 0 x NaN would
-                // reach O through P = 0
-                uint8_t* vrow = smem + kOffStage + (j & 1) * kStageBytes + kTileBytes + r * 128;
+                // reach O through P = 0.  Zero them once their TMA copy has landed.
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1))) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (j == T - 1 && r >= kv_end - j * kMqTokens) {
+                uint8_t* vrow = smem + kOffV + (j % kVStages) * kTileBytes + r * 128;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
