@@ -39,12 +39,12 @@ constexpr int kHD = 128;                              // head dim of this kernel
 constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 B (64 elements)
 constexpr int kTileBytes = 2 * kHalfBytes;            // 128 rows x 256 B
 constexpr int kOffQ = 0;
-constexpr int kKStages = 3;                           // K ring: freed when S_j completes
+constexpr int kKStages = 2;                           // K ring: freed when S_j completes
 constexpr int kVStages = 2;                           // V ring: freed when P_j V_j completes
 constexpr int kOffK = kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;
-constexpr int kOffBars = kOffP + kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;  // P double-buffered
+constexpr int kOffBars = kOffP + 2 * kTileBytes;
 constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
 constexpr int kThreads = 224;                         // 4 row warps, K and V producers, MMA
 constexpr uint32_t kTmemCols = 512;                   // S0 [0,128) S1 [128,256) O [256,384)
@@ -146,14 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sP = smem + kOffP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    uint64_t* k_full = bars;         // [3] TMA bytes of a K stage landed
-    uint64_t* k_empty = bars + 3;    // [3] the S MMA reading the K stage completed
-    uint64_t* v_full = bars + 6;     // [2] TMA bytes of a V stage landed
-    uint64_t* v_empty = bars + 8;    // [2] the P.V MMA reading the V stage completed
-    uint64_t* s_full = bars + 10;    // [2] S buffer computed
-    uint64_t* q_full = bars + 12;    // Q rows written (128 arrivals)
-    uint64_t* p_full = bars + 13;    // P written, O rescaled (128 arrivals)
-    uint64_t* o_done = bars + 14;    // the tile's P.V completed
+    uint64_t* k_full = bars;         // [2] TMA bytes of a K stage landed
+    uint64_t* k_empty = bars + 2;    // [2] the S MMA reading the K stage completed
+    uint64_t* v_full = bars + 4;     // [2] TMA bytes of a V stage landed
+    uint64_t* v_empty = bars + 6;    // [2] the P.V MMA reading the V stage completed
+    uint64_t* s_full = bars + 8;     // [2] S buffer computed
+    uint64_t* p_full = bars + 10;    // [2] P buffer written, O rescaled (128 arrivals)
+    uint64_t* o_done = bars + 12;    // [2] P_j V_j completed (P buffer j % 2 free)
+    uint64_t* q_full = bars + 14;    // Q rows written (128 arrivals)
     uint64_t* drain = bars + 15;     // every MMA of the CTA completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -195,10 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&o_done[i], 1);
+        }
         mbar_init(q_full, 128);
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -274,18 +276,19 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 if (j > 0) {
                     // O += P_{j-1} V_{j-1}
                     const int pj = j - 1, vs = pj % kVStages;
-                    if (!mbar_wait(p_full, pj & 1) ||
+                    if (!mbar_wait(&p_full[pj & 1], (pj >> 1) & 1) ||
                         !mbar_wait(&v_full[vs], (pj / kVStages) & 1)) { ok = false; break; }
                     tc5::fence_after_sync();
                     const uint32_t aV = smem_addr(smem + kOffV + vs * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t offp = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
+                        const uint32_t offp = (uint32_t)((pj & 1) * kTileBytes + (k >> 2) * kHalfBytes +
+                                                         (k & 3) * 32);
                         tc5::mma_ss(tmem + kColO, tc5::smem_desc_sw128(aP + offp, 16, 1024),
                                     tc5::smem_desc_sw128(aV + (uint32_t)(k * 2048), kHalfBytes, 1024),
                                     idpv, pj > 0 || k > 0);
                     }
-                    tc5::commit(o_done);
+                    tc5::commit(&o_done[pj & 1]);
                     tc5::commit(&v_empty[vs]);
                 }
             }
@@ -350,13 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
             const float mx = pmx[0] * p.qk_scale_log2;
             const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
-            // P and O are free once the previous tile's P.V has completed
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1))) { ok = false; break; }
-                tc5::fence_after_sync();
-            }
             const bool resc = j > 0 && m_new != m_run;
             if (__any_sync(0xffffffffu, resc)) {
+                // O may be rescaled once the previous tile's P.V has completed
+                if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc5::fence_after_sync();
                 const float f = resc ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
@@ -371,6 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 l_run *= f;
             }
             m_run = m_new;
+            // P buffer j % 2 is free once P_{j-2} V_{j-2} has completed
+            if (j > 1 &&
+                !__all_sync(0xffffffffu, mbar_wait(&o_done[j & 1], ((j - 2) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            uint8_t* sPj = sP + (j & 1) * kTileBytes;
             // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
             // operand type; l sums the weights, 8 partial sums
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     pls[(2 * e) & 7] += a;
                     pls[(2 * e + 1) & 7] += bb;
                 }
-                *reinterpret_cast<uint4*>(sP + (c8 >> 3) * kHalfBytes + sw128(r, c8 & 7)) =
+                *reinterpret_cast<uint4*>(sPj + (c8 >> 3) * kHalfBytes + sw128(r, c8 & 7)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
             float lsum = 0.f;
@@ -418,9 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             }
             fence_proxy_async_smem();
             tc5::fence_before_sync();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[j & 1]);
         }
-        if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(o_done, (T - 1) & 1));
+        if (ok)
+            ok = __all_sync(0xffffffffu, !*abort_flag &&
+                                             mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1));
         if (ok) {
             tc5::fence_after_sync();
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
