@@ -206,9 +206,13 @@ def copy_peak_gbs(torch, device, stream) -> float:
     return best
 
 
-def decode_source_hash() -> str:
+MQ_SOURCES = ["common.cuh", "tcgen05.cuh", "mq_attention.cu", "mq_attention.cuh", "tmap.cu",
+              "tmap.cuh", "api.cu"]
+
+
+def decode_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for fn in DECODE_SOURCES:
+    for fn in sources or DECODE_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_87_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -222,7 +226,8 @@ def recorded_traffic(workload):
     with open(path) as f:
         d = json.load(f)
     rec = d.get(str(workload))
-    if not rec or rec.get("source_hash") != decode_source_hash():
+    srcs = MQ_SOURCES if str(workload).startswith("mq") else None
+    if not rec or rec.get("source_hash") != decode_source_hash(srcs):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -249,8 +254,9 @@ def record_traffic(csv_path: str, workload, kernels=("decode_mma_kernel",
         raise SystemExit(f"no {'/'.join(kernels)} launch with DRAM byte counters in {csv_path}")
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     d = json.load(open(path)) if os.path.exists(path) else {}
+    srcs = MQ_SOURCES if str(workload).startswith("mq") else None
     d[str(workload)] = {"dram_bytes_per_launch": sum(per.values()) / len(per),
-                        "launches": len(per), "source_hash": decode_source_hash()}
+                        "launches": len(per), "source_hash": decode_source_hash(srcs)}
     with open(path, "w") as f:
         json.dump(d, f, indent=1, sort_keys=True)
         f.write("\n")

@@ -73,7 +73,7 @@ def test_traffic_record_requires_matching_source(tmp_path, monkeypatch):
         {"1": {"source_hash": h, "dram_bytes_per_launch": 123},
          "2": {"source_hash": "stale", "dram_bytes_per_launch": 456}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "decode_source_hash", lambda: h)
+    monkeypatch.setattr(bench, "decode_source_hash", lambda sources=None: h)
     assert bench.recorded_traffic(1) == 123
     assert bench.recorded_traffic(2) is None
     assert bench.recorded_traffic(3) is None
