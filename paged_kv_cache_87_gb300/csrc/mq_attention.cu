@@ -39,19 +39,21 @@ constexpr int kHD = 128;                              // head dim of this kernel
 constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 B (64 elements)
 constexpr int kTileBytes = 2 * kHalfBytes;            // 128 rows x 256 B
 constexpr int kOffQ = 0;
-constexpr int kKStages = 2;                           // K ring: freed when S_j completes
+constexpr int kKStages = 3;                           // K ring: freed when S_j completes
 constexpr int kVStages = 2;                           // V ring: freed when P_j V_j completes
 constexpr int kOffK = kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;  // P double-buffered
-constexpr int kOffBars = kOffP + 2 * kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;  // one P tile
+constexpr int kOffBars = kOffP + kTileBytes;
 constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
-constexpr int kThreads = 224;                         // 4 row warps, K and V producers, MMA
+constexpr int kThreads = 352;                         // 8 row warps, K and V producers, MMA
 constexpr uint32_t kTmemCols = 512;                   // S0 [0,128) S1 [128,256) O [256,384)
 constexpr uint32_t kColO = 256;
 constexpr float kMaxSlack = 8.0f;                     // log2-domain headroom before the max moves
 
 static_assert(kOffBars + 256 + 1024 <= 227 * 1024, "shared memory per CTA");
+constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 1 + 1;
+static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM slot and flag fit their region");
 
 // 16-byte chunk c (0..7) of row r of a 128B-swizzled [rows x 128 B] region.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
@@ -146,16 +148,16 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     uint8_t* sQ = smem + kOffQ;
     uint8_t* sP = smem + kOffP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    uint64_t* k_full = bars;         // [2] TMA bytes of a K stage landed
-    uint64_t* k_empty = bars + 2;    // [2] the S MMA reading the K stage completed
-    uint64_t* v_full = bars + 4;     // [2] TMA bytes of a V stage landed
-    uint64_t* v_empty = bars + 6;    // [2] the P.V MMA reading the V stage completed
-    uint64_t* s_full = bars + 8;     // [2] S buffer computed
-    uint64_t* p_full = bars + 10;    // [2] P buffer written, O rescaled (128 arrivals)
-    uint64_t* o_done = bars + 12;    // [2] P_j V_j completed (P buffer j % 2 free)
-    uint64_t* q_full = bars + 14;    // Q rows written (128 arrivals)
-    uint64_t* drain = bars + 15;     // every MMA of the CTA completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+    uint64_t* k_full = bars;                     // [kKStages] TMA bytes of a K stage landed
+    uint64_t* k_empty = k_full + kKStages;       // [kKStages] the S MMA reading it completed
+    uint64_t* v_full = k_empty + kKStages;       // [kVStages] TMA bytes of a V stage landed
+    uint64_t* v_empty = v_full + kVStages;       // [kVStages] the P.V MMA reading it completed
+    uint64_t* s_full = v_empty + kVStages;       // [2] S buffer computed
+    uint64_t* p_full = s_full + 2;               // [2] P tile written, O rescaled (256 arrivals)
+    uint64_t* o_done = p_full + 2;               // [2] P_j V_j completed (by tile parity)
+    uint64_t* q_full = o_done + 2;               // Q rows written (256 arrivals)
+    uint64_t* drain = q_full + 1;                // every MMA of the CTA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,23 +199,23 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
+            mbar_init(&p_full[i], 256);
             mbar_init(&o_done[i], 1);
         }
-        mbar_init(q_full, 128);
+        mbar_init(q_full, 256);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tc5::tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 10) tc5::tmem_alloc(tmem_slot, kTmemCols);
     tc5::fence_before_sync();
     __syncthreads();
     tc5::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4 || warp == 6) {
-        // ===================== TMA producers: warp 4 K, warp 6 V =====================
-        const bool isK = warp == 4;
+    if (warp == 8 || warp == 9) {
+        // ===================== TMA producers: warp 8 K, warp 9 V =====================
+        const bool isK = warp == 8;
         const CUtensorMap* map = isK ? &tmK : &tmV;
         if (lane == 0) prefetch_tensormap(map);
         const uint64_t policy = l2_evict_last_policy();   // other row tiles re-read K/V
@@ -223,6 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         uint64_t* empty = isK ? k_empty : v_empty;
         uint8_t* ring = smem + (isK ? kOffK : kOffV);
         const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
+        const int nb_all = (kv_end + B - 1) / B;          // table entries this CTA reads
+        // block-table window: lane l holds entry wb + l (cur) and wb + 32 + l (nxt); the
+        // next window loads as soon as the current one is entered, so a tile's entries
+        // are in registers when its stage frees (a tile spans <= 16 entries)
+        int wb = 0;
+        int cur = lane < nb_all ? trow[lane] : 0;
+        int nxt = lane + 32 < nb_all ? trow[lane + 32] : 0;
         for (int j = 0; j < T; ++j) {
             const int st = j % nst;
             if (!mbar_wait(&empty[st], ((j / nst) & 1) ^ 1u)) {
@@ -232,10 +241,20 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             }
             const int t0 = j * kMqTokens, t1 = min(t0 + kMqTokens, kv_end);
             const int fb = t0 / B, nblk = (t1 - 1) / B - fb + 1;   // <= 128 / B <= 16
+            if (fb >= wb + 32) {                          // warp-uniform: enter the next window
+                wb += 32;
+                cur = nxt;
+                nxt = wb + 32 + lane < nb_all ? trow[wb + 32 + lane] : 0;
+            }
             if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nblk * B) * 256u);
             __syncwarp();
+            const int src = fb + lane - wb;               // fb - wb < 32, lane < nblk <= 16
+            int phys = __shfl_sync(0xffffffffu, cur, src & 31);
+            if (fb + nblk > wb + 32) {                    // warp-uniform: the tile straddles
+                const int hi = __shfl_sync(0xffffffffu, nxt, src & 31);
+                if (src >= 32) phys = hi;
+            }
             if (lane < nblk) {
-                int phys = trow[fb + lane];
                 if (phys < 0 || phys >= p.num_blocks) {
                     if (isK) set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
                     phys = 0;
@@ -246,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 tma_load_2d(dst + kHalfBytes, map, 64, y, &full[st], policy);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 10) {
         // ============================ MMA issuer =============================
         if (lane == 0) {
             constexpr bool kBF16 = std::is_same<QT, BF16>::value;
@@ -282,8 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     const uint32_t aV = smem_addr(smem + kOffV + vs * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t offp = (uint32_t)((pj & 1) * kTileBytes + (k >> 2) * kHalfBytes +
-                                                         (k & 3) * 32);
+                        const uint32_t offp = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
                         tc5::mma_ss(tmem + kColO, tc5::smem_desc_sw128(aP + offp, 16, 1024),
                                     tc5::smem_desc_sw128(aV + (uint32_t)(k * 2048), kHalfBytes, 1024),
                                     idpv, pj > 0 || k > 0);
@@ -302,24 +320,29 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         }
         __syncwarp();
     } else {
-        // ================= rows: Q, softmax, O rescale, epilogue =================
-        const int r = threadIdx.x;                        // TMEM lane = row
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // ======= rows: Q, softmax, O rescale, epilogue; two threads per row =======
+        // warps 4h .. 4h+3 take columns [64 h, 64 h + 64) of every S tile, of P and of
+        // O (and half h of d for Q and the output); both threads of a row read all 128
+        // scores for the row max, so they agree on it without exchanging anything
+        const int half = warp >> 2;
+        const int r = threadIdx.x & (kMqRows - 1);        // TMEM lane = row
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int qi = q0 + r / G, hq = kvh * G + r % G;
         const bool row_valid = r < rows_valid;
         const int64_t qrow = ((int64_t)(q_begin + qi) * p.num_q_heads + hq) * kHD;
         {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                              (row_valid ? qrow : 0));
+                                                              (row_valid ? qrow : 0)) + 8 * half;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
+            for (int c = 0; c < 8; ++c) {
                 const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sQ + (c >> 3) * kHalfBytes + sw128(r, c & 7)) = v;
+                *reinterpret_cast<uint4*>(sQ + half * kHalfBytes + sw128(r, c)) = v;
             }
             fence_proxy_async_smem();
             mbar_arrive(q_full);
         }
         const int pos_r = pos0 + r / G;                   // this row's query position
+        const uint32_t colS0 = lane_base, colOh = lane_base + kColO + (uint32_t)(64 * half);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < T; ++j) {
@@ -328,27 +351,37 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             const bool got = !*abort_flag && mbar_wait(&s_full[j & 1], (j >> 1) & 1);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             tc5::fence_after_sync();
-            uint32_t sv[4][32];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                tc5::ld_32x32b_x32(tmem + lane_base + (uint32_t)((j & 1) * 128 + c4 * 32), sv[c4]);
-            tc5::wait_ld();
-            // local tokens <= lim are visible (rows past the last query see no further)
-            const int lim = min(pos_r, kv_end - 1) - j * kMqTokens;
+            const uint32_t colS = colS0 + (uint32_t)((j & 1) * 128);
+            // local tokens <= lim are visible (rows past the last query see no further);
             // a tile every row of the warp sees whole needs no mask
-            if (!__all_sync(0xffffffffu, lim >= kMqTokens - 1)) {
+            const int lim = min(pos_r, kv_end - 1) - j * kMqTokens;
+            const bool masked = !__all_sync(0xffffffffu, lim >= kMqTokens - 1);
+            // this thread's 64 scores, kept for P
+            uint32_t sv[2][32];
+            tc5::ld_32x32b_x32(colS + (uint32_t)(64 * half), sv[0]);
+            tc5::ld_32x32b_x32(colS + (uint32_t)(64 * half + 32), sv[1]);
+            // the other half's 64, only for the row max
+            uint32_t so[2][32];
+            tc5::ld_32x32b_x32(colS + (uint32_t)(64 * (1 - half)), so[0]);
+            tc5::ld_32x32b_x32(colS + (uint32_t)(64 * (1 - half) + 32), so[1]);
+            tc5::wait_ld();
+            if (masked) {
 #pragma unroll
-                for (int c = 0; c < kMqTokens; ++c)
-                    if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 64; ++c) {
+                    if (64 * half + c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                    if (64 * (1 - half) + c > lim) so[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                }
             }
             // row max of the raw scores (the scale is positive: same order), with 8
-            // independent partial maxima instead of one 128-long chain
+            // independent partial maxima
             float pmx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) pmx[i] = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kMqTokens; ++c)
+            for (int c = 0; c < 64; ++c) {
                 pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(sv[c >> 5][c & 31]));
+                pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(so[c >> 5][c & 31]));
+            }
 #pragma unroll
             for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
             const float mx = pmx[0] * p.qk_scale_log2;
@@ -363,69 +396,68 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 tc5::fence_after_sync();
                 const float f = resc ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
+                for (int c4 = 0; c4 < 2; ++c4) {
                     uint32_t o[32];
-                    tc5::ld_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                    tc5::ld_32x32b_x32(colOh + (uint32_t)(c4 * 32), o);
                     tc5::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tc5::st_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                    tc5::st_32x32b_x32(colOh + (uint32_t)(c4 * 32), o);
                 }
                 tc5::wait_st();
                 l_run *= f;
             }
             m_run = m_new;
-            // P buffer j % 2 is free once P_{j-2} V_{j-2} has completed
-            if (j > 1 &&
-                !__all_sync(0xffffffffu, mbar_wait(&o_done[j & 1], ((j - 2) >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            uint8_t* sPj = sP + (j & 1) * kTileBytes;
+            // the P tile is free once P_{j-1} V_{j-1} has completed: the weights are
+            // computed into registers first, the wait comes just before the stores
+            uint8_t* sPj = sP + half * kHalfBytes;
             // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
-            // operand type; l sums the weights, 8 partial sums
+            // operand type; l sums this thread's weights, 8 partial sums
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
             float pls[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) pls[i] = 0.f;
+            uint32_t pw[32];                              // this thread's 64 weights, packed
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c8 * 8 + 2 * e;
-                    const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
-                                                   p.qk_scale_log2, neg_m));
-                    const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
-                                                    p.qk_scale_log2, neg_m));
-                    w[e] = pack2_bits<QT>(a, bb);
-                    pls[(2 * e) & 7] += a;
-                    pls[(2 * e + 1) & 7] += bb;
-                }
-                *reinterpret_cast<uint4*>(sPj + (c8 >> 3) * kHalfBytes + sw128(r, c8 & 7)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 32; ++e) {
+                const int c = 2 * e;
+                const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
+                                               p.qk_scale_log2, neg_m));
+                const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
+                                                p.qk_scale_log2, neg_m));
+                pw[e] = pack2_bits<QT>(a, bb);
+                pls[(2 * e) & 7] += a;
+                pls[(2 * e + 1) & 7] += bb;
             }
+            if (j > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                *reinterpret_cast<uint4*>(sPj + sw128(r, c8)) =
+                    make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
             float lsum = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) lsum += pls[i];
             l_run += lsum;
             if (j == T - 1 && kv_end - j * kMqTokens < kMqTokens) {
                 // V rows past the last token hold poison or stale data: 0 x NaN would
-                // reach O through P = 0.  Zero them once their TMA copy has landed.
+                // reach O through P = 0.  Zero them (this thread's half of d) once their
+                // TMA copy has landed.
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1))) {
                     ok = false;
                     break;
                 }
-            }
-            if (j == T - 1 && r >= kv_end - j * kMqTokens) {
-                uint8_t* vrow = smem + kOffV + (j % kVStages) * kTileBytes + r * 128;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
+                if (r >= kv_end - j * kMqTokens) {
+                    uint8_t* vrow = smem + kOffV + (j % kVStages) * kTileBytes + half * kHalfBytes +
+                                    r * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(vrow + h * kHalfBytes + c * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             fence_proxy_async_smem();
             tc5::fence_before_sync();
@@ -434,13 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         if (ok)
             ok = __all_sync(0xffffffffu, !*abort_flag &&
                                              mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1));
+        // the row's softmax denominator: the two threads' sums, exchanged through the
+        // first P buffer (every P.V has completed); all 256 row threads take part
+        float* xl = reinterpret_cast<float*>(sP);
+        xl[half * kMqRows + r] = l_run;
+        named_bar_sync(1, 2 * kMqRows);
+        const float l_row = xl[r] + xl[kMqRows + r];
         if (ok) {
             tc5::fence_after_sync();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c4 = 0; c4 < 2; ++c4) {
                 uint32_t o[32];
-                tc5::ld_32x32b_x32(tmem + lane_base + kColO + (uint32_t)(c4 * 32), o);
+                tc5::ld_32x32b_x32(colOh + (uint32_t)(c4 * 32), o);
                 tc5::wait_ld();
                 if (row_valid) {
                     uint32_t w[16];
@@ -451,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                                          __uint_as_float(o[2 * e + 1]) * inv, ra, rb);
                     }
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow +
-                                                          c4 * 32);
+                                                          64 * half + c4 * 32);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
@@ -464,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     }
     tc5::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 10) {
         tc5::fence_after_sync();
         tc5::tmem_dealloc(tmem, kTmemCols);
     }
