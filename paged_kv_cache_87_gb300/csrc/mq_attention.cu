@@ -38,17 +38,24 @@ namespace {
 constexpr int kHD = 128;                              // head dim of this kernel
 constexpr int kHalfBytes = 128 * 128;                 // 128 rows x 128 B (64 elements)
 constexpr int kTileBytes = 2 * kHalfBytes;            // 128 rows x 256 B
-constexpr int kOffQ = 0;
-constexpr int kKStages = 3;                           // K ring: freed when S_j completes
-constexpr int kVStages = 2;                           // V ring: freed when P_j V_j completes
-constexpr int kOffK = kTileBytes;
+// K and V tiles arrive as [group of 8 tokens][half of d][8 tokens][128 B]
+constexpr int kGroupHalf = 8 * 128;                   // one half of d of an 8-token group
+constexpr int kGroupBytes = 2 * kGroupHalf;           // an 8-token group
+constexpr int kKStages = 4;                           // K ring: freed when S_j completes
+constexpr int kVStages = 3;                           // V ring: freed when P_j V_j completes
+constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;  // one P tile
-constexpr int kOffBars = kOffP + kTileBytes;
+constexpr int kOffX = kOffV + kVStages * kTileBytes;  // the rows' softmax sums, exchanged
+constexpr int kOffBars = kOffX + 1024;
 constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
 constexpr int kThreads = 352;                         // 8 row warps, K and V producers, MMA
-constexpr uint32_t kTmemCols = 512;                   // S0 [0,128) S1 [128,256) O [256,384)
+// TMEM columns (lane = row): S double-buffered (fp32), O (fp32), and the MMA A
+// operands Q and P (16-bit, two elements per column)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;                         // S_j at kColS + 128 (j % 2)
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColQ = 384;
+constexpr uint32_t kColP = 448;
 constexpr float kMaxSlack = 8.0f;                     // log2-domain headroom before the max moves
 
 static_assert(kOffBars + 256 + 1024 <= 227 * 1024, "shared memory per CTA");
@@ -145,8 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem + kOffQ;
-    uint8_t* sP = smem + kOffP;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* k_full = bars;                     // [kKStages] TMA bytes of a K stage landed
     uint64_t* k_empty = k_full + kKStages;       // [kKStages] the S MMA reading it completed
@@ -259,10 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     if (isK) set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
                     phys = 0;
                 }
+                // one box per block: both 128-byte halves of its B rows, landing as
+                // [group of 8 rows][half][8 rows][128 B] at the block's place in the tile
                 const int y = (phys * p.num_kv_heads + kvh) * B;
-                uint8_t* dst = ring + st * kTileBytes + lane * B * 128;
-                tma_load_2d(dst, map, 0, y, &full[st], policy);
-                tma_load_2d(dst + kHalfBytes, map, 64, y, &full[st], policy);
+                uint8_t* dst = ring + st * kTileBytes + lane * B * 256;
+                tc5::tma_load_4d(dst, map, 0, 0, 0, y >> 3, &full[st], policy);
             }
         }
     } else if (warp == 10) {
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             constexpr bool kBF16 = std::is_same<QT, BF16>::value;
             constexpr uint32_t idqk = tc5::idesc_f16(kBF16, 128, 128, false, false);
             constexpr uint32_t idpv = tc5::idesc_f16(kBF16, 128, 128, false, true);
-            const uint32_t aQ = smem_addr(sQ), aP = smem_addr(sP);
+
             bool ok = mbar_wait(q_full, 0);
             tc5::fence_after_sync();
             for (int j = 0; j <= T && ok; ++j) {
@@ -284,10 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     const uint32_t aK = smem_addr(smem + kOffK + ks * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t off = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
-                        tc5::mma_ss(tmem + (uint32_t)(st * 128),
-                                    tc5::smem_desc_sw128(aQ + off, 16, 1024),
-                                    tc5::smem_desc_sw128(aK + off, 16, 1024), idqk, k > 0);
+                        const uint32_t offk = (uint32_t)((k >> 2) * kGroupHalf + (k & 3) * 32);
+                        tc5::mma_ts(tmem + kColS + (uint32_t)(st * 128),
+                                    tmem + kColQ + (uint32_t)(8 * k),
+                                    tc5::smem_desc_sw128(aK + offk, 16, kGroupBytes), idqk, k > 0);
                     }
                     tc5::commit(&s_full[st]);
                     tc5::commit(&k_empty[ks]);
@@ -301,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     const uint32_t aV = smem_addr(smem + kOffV + vs * kTileBytes);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t offp = (uint32_t)((k >> 2) * kHalfBytes + (k & 3) * 32);
-                        tc5::mma_ss(tmem + kColO, tc5::smem_desc_sw128(aP + offp, 16, 1024),
-                                    tc5::smem_desc_sw128(aV + (uint32_t)(k * 2048), kHalfBytes, 1024),
+                        tc5::mma_ts(tmem + kColO, tmem + kColP + (uint32_t)(8 * k),
+                                    tc5::smem_desc_sw128(aV + (uint32_t)(k * 2 * kGroupBytes),
+                                                         kGroupHalf, kGroupBytes),
                                     idpv, pj > 0 || k > 0);
                     }
                     tc5::commit(&o_done[pj & 1]);
@@ -331,18 +337,26 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         const bool row_valid = r < rows_valid;
         const int64_t qrow = ((int64_t)(q_begin + qi) * p.num_q_heads + hq) * kHD;
         {
+            // this thread's half of the row's q, packed two per column, into TMEM
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                               (row_valid ? qrow : 0)) + 8 * half;
+            uint32_t qw[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sQ + half * kHalfBytes + sw128(r, c)) = v;
+                qw[4 * c] = v.x;
+                qw[4 * c + 1] = v.y;
+                qw[4 * c + 2] = v.z;
+                qw[4 * c + 3] = v.w;
             }
-            fence_proxy_async_smem();
+            tc5::st_32x32b_x32(lane_base + tmem + kColQ + (uint32_t)(32 * half), qw);
+            tc5::wait_st();
+            tc5::fence_before_sync();
             mbar_arrive(q_full);
         }
         const int pos_r = pos0 + r / G;                   // this row's query position
-        const uint32_t colS0 = lane_base, colOh = lane_base + kColO + (uint32_t)(64 * half);
+        const uint32_t colS0 = tmem + lane_base + kColS,
+                       colOh = tmem + lane_base + kColO + (uint32_t)(64 * half);
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < T; ++j) {
@@ -408,9 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 l_run *= f;
             }
             m_run = m_new;
-            // the P tile is free once P_{j-1} V_{j-1} has completed: the weights are
-            // computed into registers first, the wait comes just before the stores
-            uint8_t* sPj = sP + half * kHalfBytes;
+            // the P columns are free once P_{j-1} V_{j-1} has completed: the weights
+            // are computed into registers first, the wait comes just before the store
             // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
             // operand type; l sums this thread's weights, 8 partial sums
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
@@ -434,10 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 ok = false;
                 break;
             }
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4*>(sPj + sw128(r, c8)) =
-                    make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
+            tc5::fence_after_sync();
+            tc5::st_32x32b_x32(tmem + lane_base + kColP + (uint32_t)(32 * half), pw);
             float lsum = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) lsum += pls[i];
@@ -452,23 +463,24 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     break;
                 }
                 if (r >= kv_end - j * kMqTokens) {
-                    uint8_t* vrow = smem + kOffV + (j % kVStages) * kTileBytes + half * kHalfBytes +
-                                    r * 128;
+                    uint8_t* vrow = smem + kOffV + (j % kVStages) * kTileBytes +
+                                    (r >> 3) * kGroupBytes + half * kGroupHalf + (r & 7) * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            fence_proxy_async_smem();
+            tc5::wait_st();
+            fence_proxy_async_smem();                     // the V rows zeroed above
             tc5::fence_before_sync();
             mbar_arrive(&p_full[j & 1]);
         }
         if (ok)
             ok = __all_sync(0xffffffffu, !*abort_flag &&
                                              mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1));
-        // the row's softmax denominator: the two threads' sums, exchanged through the
-        // first P buffer (every P.V has completed); all 256 row threads take part
-        float* xl = reinterpret_cast<float*>(sP);
+        // the row's softmax denominator: the two threads' sums, exchanged through
+        // shared memory; all 256 row threads take part
+        float* xl = reinterpret_cast<float*>(smem + kOffX);
         xl[half * kMqRows + r] = l_run;
         named_bar_sync(1, 2 * kMqRows);
         const float l_row = xl[r] + xl[kMqRows + r];
@@ -523,8 +535,8 @@ cudaError_t launch_typed(const MqParams& p, int64_t max_items, cudaStream_t stre
     }
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
-    if (!encode_pool_map(&tk, p.k_cache, kHD, 2, rows, p.block_size) ||
-        !encode_pool_map(&tv, p.v_cache, kHD, 2, rows, p.block_size))
+    if (!encode_pool_map_grouped(&tk, p.k_cache, rows, p.block_size) ||
+        !encode_pool_map_grouped(&tv, p.v_cache, rows, p.block_size))
         return cudaErrorInvalidValue;
     mq_plan_kernel<<<1, 1024, 0, stream>>>(p);
     err = cudaGetLastError();

@@ -73,12 +73,39 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]^T for one M x N x 16 step: A's M rows are TMEM
+// lanes, its 16 K elements (16-bit) packed two per 32-bit column, 8 columns from
+// `a_tmem`; issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // The mbarrier at `bar` receives one arrival when every tcgen05 operation this
 // thread issued before has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
         ::"r"(smem_addr(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------- TMA 4-D --
+
+// 4-D TMA tile load global -> shared, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int c0,
+                                            int c1, int c2, int c3, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(c2), "r"(c3), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
 }
 
 // ------------------------------------------------------------ TMEM <-> RF --

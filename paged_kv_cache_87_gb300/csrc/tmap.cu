@@ -51,4 +51,20 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int head_dim, int elem_
            CUDA_SUCCESS;
 }
 
+bool encode_pool_map_grouped(CUtensorMap* map, const void* pool, long long rows, int box_rows) {
+    EncodeTiled enc = encoder();
+    if (!enc || rows <= 0 || rows % 8 != 0 || rows / 8 > 0x7fffffffLL || box_rows % 8 != 0)
+        return false;
+    // 16-bit rows of 128 elements viewed as (64 elements, 8 rows, 2 halves, rows / 8):
+    // a box of box_rows rows lands as [group of 8 rows][half][8 rows][128 bytes]
+    const cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+    const cuuint64_t strides[3] = {256, 128, 2048};
+    const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(box_rows / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(pool), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace pkv

@@ -10,4 +10,10 @@ namespace pkv {
 bool encode_pool_map(CUtensorMap* map, const void* pool, int head_dim, int elem_bytes,
                      long long rows, int box_rows);
 
+// The same pool for 16-bit rows of 128 elements as a 4-D tensor (64 elements,
+// 8 rows, 2 halves, row groups): one box of box_rows (a multiple of 8) rows carries
+// both 128-byte halves and lands as [group of 8 rows][half][8 rows][128 B], 128-byte
+// swizzled, so the 8-row groups of a half are 2 KB apart across blocks.
+bool encode_pool_map_grouped(CUtensorMap* map, const void* pool, long long rows, int box_rows);
+
 }  // namespace pkv
