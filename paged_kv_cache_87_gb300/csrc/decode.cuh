@@ -45,6 +45,15 @@ constexpr int kGroupRecord = 1 << 30;  // record code flag: a shared-prefix grou
 constexpr int kMaxGroupHeads = 16;     // query heads a shared-prefix unit serves
 constexpr int kTileTokens = 64;        // split granularity of the balanced split
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel on its stream still runs;
+// pdl_wait blocks until that kernel has completed and its memory is visible.
+// pdl_launch_dependents lets the next such kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 struct DecodeWork {
     unsigned* counter;    // next work index (dynamic items)
     unsigned* total;      // number of work indices (dynamic items)

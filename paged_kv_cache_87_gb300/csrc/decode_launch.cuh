@@ -79,12 +79,25 @@ cudaError_t launch_decode_mma_nt(const DecodeParams& p, cudaStream_t stream) {
     plan_split_kernel<QT><<<1, 1024, 0, stream>>>(ps);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    kernel<<<ps.num_workers, Cfg::THREADS, Cfg::SMEM, stream>>>(ps, tk, tv);
-    err = cudaGetLastError();
+    // the decode (and merge) kernels start launching while their predecessor runs
+    // and wait for it on the device (programmatic dependent launch)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ps.num_workers, 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, ps, tk, tv);
     if (err != cudaSuccess || !ps.allow_groups) return err;
     const int units = ps.num_seqs * ps.num_kv_heads * ps.nsub;
-    merge_units_kernel<QT, HD><<<(units + 7) / 8, 256, 0, stream>>>(ps);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)((units + 7) / 8), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, merge_units_kernel<QT, HD>, ps);
 }
 
 template <typename QT, typename KT, int HD>

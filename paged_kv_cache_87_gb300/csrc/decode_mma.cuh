@@ -205,6 +205,7 @@ __device__ __forceinline__ void scan2(int a, int b, int* ex_a, int* ex_b, int* t
 //     start.  Unit counters reset; outputs of empty sequences zeroed.
 template <typename QT>
 __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
+    pdl_launch_dependents();   // the decode kernel's prologue overlaps this plan
     __shared__ int s_ctx[1024], s_first[1024], s_run[1024], s_mem[1024], s_sh[1024];
     __shared__ int wa[32], wb[32];
     __shared__ int carry_rec, carry_tiles;
@@ -497,6 +498,7 @@ __device__ __forceinline__ void merge_unit_warp(const DecodeParams& p, int64_t r
 // Ungrouped units whose context fits one segment were written directly.
 template <typename QT, int HD>
 __global__ void __launch_bounds__(256) merge_units_kernel(DecodeParams p) {
+    pdl_wait();                                           // every partial state is written
     const int upi = p.num_kv_heads * p.nsub;
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (w >= p.num_seqs * upi) return;
@@ -646,6 +648,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     __syncthreads();
 
     const int B = p.block_size;
+    pdl_wait();                                           // the planning kernel has completed
     const int q = p.ws.quota[0], total = p.ws.quota[1];   // written by the planning kernel
     const int a = blockIdx.x * q, end = min(a + q, total);
 
