@@ -7,7 +7,7 @@
 
 namespace pkv {
 
-constexpr int kMqRows = 128;     // (query token, head of the group) rows per CTA tile
+constexpr int kMqRows = 256;     // (query token, head of the group) rows per CTA: two tiles of 128
 constexpr int kMqTokens = 128;   // K/V tokens per pipeline tile
 
 struct MqParams {

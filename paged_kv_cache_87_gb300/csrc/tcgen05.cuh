@@ -108,6 +108,22 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// ------------------------------------------------------ register split --
+
+// Every warp of a warpgroup executes the same one: lowers (dec) or raises (inc)
+// the warpgroup's registers per thread; the raises wait for registers that
+// other warpgroups released.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg operand");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------ TMEM <-> RF --
 
 // Warp-wide: lane i reads 32 consecutive 32-bit columns of TMEM lane
