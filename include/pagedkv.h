@@ -196,8 +196,11 @@ PKV_API pkv_status pkv_paged_decode_attention_prefix(
  * divisor of 128; others return PKV_ERR_UNSUPPORTED.  Q K^T and P V run on the
  * tcgen05 tensor cores with fp32 accumulation in tensor memory; P is rounded
  * to q_dtype before P V (the softmax denominator sums the fp32 weights).
- * Two launches on `stream`: a one-CTA planning kernel and the attention
- * kernel (one CTA per sequence, kv head and 128 (query, head) rows).
+ * Two launches on `stream`: a one-CTA planning kernel (it orders the
+ * sequences by context length, longest first, when there are at most 1024)
+ * and the attention kernel (one CTA per sequence, kv head and 256
+ * (query, head) rows, launched in that order).  The workspace holds the
+ * plan: per-sequence CTA offsets and the launch order.
  */
 PKV_API size_t pkv_multi_query_workspace_bytes(int num_seqs);
 

@@ -375,7 +375,7 @@ int pkv_version(void) { return 100; }
 
 size_t pkv_multi_query_workspace_bytes(int num_seqs) {
     if (num_seqs < 0) return 0;
-    return round_up(((size_t)num_seqs + 1) * 4, 256);
+    return round_up(((size_t)num_seqs + 1) * 4, 256) + round_up((size_t)num_seqs * 4, 256);
 }
 
 pkv_status pkv_paged_multi_query_attention(
@@ -419,6 +419,8 @@ pkv_status pkv_paged_multi_query_attention(
     p.query_start = query_start;
     p.out = out;
     p.item_prefix = static_cast<int*>(workspace);
+    p.seq_order = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                         round_up(((size_t)num_seqs + 1) * 4, 256));
     p.status = dev->status;
     p.num_seqs = num_seqs;
     p.total_q = total_q;

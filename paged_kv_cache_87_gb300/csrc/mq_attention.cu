@@ -105,11 +105,16 @@ __device__ __forceinline__ uint32_t pack2_bits(float a, float b) {
     }
 }
 
-// Items: per sequence ceil(n * G / 128) row tiles times Hkv; exclusive prefix.
+// Items: per sequence ceil(n * G / 256) row pairs times Hkv, the sequences taken
+// longest context first (up to kMqSortSeqs sequences; beyond, in index order) so
+// that the block scheduler hands out the longest CTAs first; exclusive prefix.
+constexpr int kMqSortSeqs = 1024;
+
 __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
     const int total_q = p.total_q;
     __shared__ int wsum[32];
     __shared__ int carry;
+    __shared__ int ctx_s[kMqSortSeqs];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         carry = 0;
@@ -117,11 +122,29 @@ __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
             set_status(p.status, PKV_DEV_BAD_CONTEXT);
     }
     const int cap = min(p.max_context_len, p.max_blocks * p.block_size);
+    // seq_order[k] = the sequence launched k-th: by context length, descending, ties
+    // by index (a rank sort)
+    if (p.num_seqs <= kMqSortSeqs) {
+        for (int s = tid; s < p.num_seqs; s += blockDim.x) ctx_s[s] = p.context_lens[s];
+        __syncthreads();
+        for (int s = tid; s < p.num_seqs; s += blockDim.x) {
+            const int c = ctx_s[s];
+            int rank = 0;
+            for (int t = 0; t < p.num_seqs; ++t) {
+                const int ct = ctx_s[t];
+                rank += (ct > c) || (ct == c && t < s);
+            }
+            p.seq_order[rank] = s;
+        }
+    } else {
+        for (int s = tid; s < p.num_seqs; s += blockDim.x) p.seq_order[s] = s;
+    }
     __syncthreads();
     for (int base = 0; base < p.num_seqs; base += blockDim.x) {
-        const int s = base + tid;
+        const int k = base + tid;
+        const int s = k < p.num_seqs ? p.seq_order[k] : 0;
         int items = 0;
-        if (s < p.num_seqs) {
+        if (k < p.num_seqs) {
             const int n = p.query_start[s + 1] - p.query_start[s];
             const int ctx = p.context_lens[s];
             if (n < 0 || ctx < n || ctx > cap || p.query_start[s] < 0 ||
@@ -150,7 +173,7 @@ __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
         }
         __syncthreads();
         const int incl = x + (warp > 0 ? wsum[warp - 1] : 0);
-        if (s < p.num_seqs) p.item_prefix[s] = carry + incl - items;
+        if (k < p.num_seqs) p.item_prefix[k] = carry + incl - items;
         __syncthreads();
         if (tid == blockDim.x - 1) carry += incl;
         __syncthreads();
@@ -316,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- this CTA's item: the last sequence whose first item is <= blockIdx.x ----
+    // ---- this CTA's item: in launch order, the last sequence whose first item is
+    // <= blockIdx.x ----
     const int b = blockIdx.x;
     if (b >= p.item_prefix[p.num_seqs]) return;   // whole CTA, before any allocation
     int lo = 0, hi = p.num_seqs - 1;
@@ -325,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         if (p.item_prefix[mid] <= b) lo = mid;
         else hi = mid - 1;
     }
-    const int s = lo;
-    const int local = b - p.item_prefix[s];
+    const int s = p.seq_order[lo];
+    const int local = b - p.item_prefix[lo];
     const int G = p.group;
     const int q_begin = p.query_start[s];
     const int n = p.query_start[s + 1] - q_begin;

@@ -8,7 +8,6 @@
 namespace pkv {
 
 constexpr int kMqRows = 256;     // (query token, head of the group) rows per CTA: two tiles of 128
-constexpr int kMqTokens = 128;   // K/V tokens per pipeline tile
 
 struct MqParams {
     const void* q;                 // [total_q, Hq, d]
@@ -18,7 +17,8 @@ struct MqParams {
     const int32_t* context_lens;   // [S]: tokens in the cache, the queries' own included
     const int32_t* query_start;    // [S + 1]: query rows of sequence s
     void* out;                     // [total_q, Hq, d]
-    int* item_prefix;              // workspace [S + 1]: (seq, kv head, row tile) items
+    int* item_prefix;              // workspace [S + 1]: items before the k-th launched sequence
+    int* seq_order;                // workspace [S]: the sequence launched k-th
     unsigned* status;
     int num_seqs, total_q, num_q_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
     int max_blocks;
