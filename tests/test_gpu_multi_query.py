@@ -192,3 +192,36 @@ def test_chunked_prefill_workload_sampled():
     ref = _oracle(w, sel=sel)
     err = np.abs(got[sel[:, 0], sel[:, 1]] - ref).max()
     assert err <= TOL["bf16"], err
+
+
+def test_more_sequences_than_the_planner_ranks():
+    """Above 1024 sequences the planner launches them in index order instead of by
+    context length; results must not depend on it."""
+    rng = np.random.default_rng(29)
+    S = 1100
+    w = inputs.make_multi_query("many", rng, rng.integers(0, 41, size=S), rng.integers(1, 4, size=S),
+                                num_q_heads=4, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype="bf16")
+    _check(w)
+
+
+def test_launch_order_leaves_every_sequence_bit_identical():
+    """The CTAs of each sequence compute the same values whatever position the planner
+    gives the sequence: permuting the sequences permutes the output rows, bit for bit."""
+    rng = np.random.default_rng(30)
+    w = inputs.make_multi_query("order", rng, [700, 3, 260, 1500, 90, 1100], [40, 9, 130, 3, 77, 256],
+                                num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype="bf16")
+    a = _gpu(w).out.clone()
+    perm = np.array([3, 0, 5, 2, 4, 1])
+    qs = w.query_start
+    rows = np.concatenate([np.arange(qs[s], qs[s + 1]) for s in perm])
+    n = np.diff(qs)[perm]
+    w2 = inputs.MultiQueryWorkload(**{**w.__dict__, "query": w.query[rows],
+                                      "block_tables": w.block_tables[perm],
+                                      "context_lens": w.context_lens[perm],
+                                      "query_start": np.concatenate([[0], np.cumsum(n)]).astype(np.int32),
+                                      "seq_tokens": [w.seq_tokens[s] for s in perm]})
+    b = _gpu(w2).out
+    assert binding.pkv_get_device_status() == 0
+    assert torch.equal(a[torch.from_numpy(rows).to(a.device)], b)
