@@ -198,9 +198,10 @@ PKV_API pkv_status pkv_paged_decode_attention_prefix(
  * to q_dtype before P V (the softmax denominator sums the fp32 weights).
  * Two launches on `stream`: a one-CTA planning kernel (it orders the
  * sequences by context length, longest first, when there are at most 1024)
- * and the attention kernel (one CTA per sequence, kv head and 256
- * (query, head) rows, launched in that order).  The workspace holds the
- * plan: per-sequence CTA offsets and the launch order.
+ * and the attention kernel: one persistent CTA per SM, each taking work
+ * items (a sequence, a kv head and 256 (query, head) rows) in that order
+ * from a counter.  The workspace holds the plan: per-sequence item offsets,
+ * the order and the counter.
  */
 PKV_API size_t pkv_multi_query_workspace_bytes(int num_seqs);
 

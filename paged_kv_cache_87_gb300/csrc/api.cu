@@ -375,7 +375,7 @@ int pkv_version(void) { return 100; }
 
 size_t pkv_multi_query_workspace_bytes(int num_seqs) {
     if (num_seqs < 0) return 0;
-    return round_up(((size_t)num_seqs + 1) * 4, 256) + round_up((size_t)num_seqs * 4, 256);
+    return round_up(((size_t)num_seqs + 1) * 4, 256) + round_up((size_t)num_seqs * 4, 256) + 256;
 }
 
 pkv_status pkv_paged_multi_query_attention(
@@ -421,6 +421,9 @@ pkv_status pkv_paged_multi_query_attention(
     p.item_prefix = static_cast<int*>(workspace);
     p.seq_order = reinterpret_cast<int*>(static_cast<char*>(workspace) +
                                          round_up(((size_t)num_seqs + 1) * 4, 256));
+    p.work_next = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                         round_up(((size_t)num_seqs + 1) * 4, 256) +
+                                         round_up((size_t)num_seqs * 4, 256));
     p.status = dev->status;
     p.num_seqs = num_seqs;
     p.total_q = total_q;
@@ -434,7 +437,7 @@ pkv_status pkv_paged_multi_query_attention(
     p.max_context_len = max_context_len;
     p.qk_scale_log2 = scale * 1.4426950408889634f;
     const int64_t items = mq_max_items(num_seqs, total_q, group, num_kv_heads);
-    return cuda_status(launch_mq_attention(p, q_dtype, items,
+    return cuda_status(launch_mq_attention(p, q_dtype, items, dev->num_sms,
                                            static_cast<cudaStream_t>(stream)));
 }
 

@@ -11,16 +11,21 @@
 // Query row i of sequence s (query_start[s] + i) is the token at position
 // ctx_s - n_s + i and attends to tokens 0 .. ctx_s - n_s + i.
 //
-// Organisation: one CTA per (sequence, kv head, 256 rows), a row being a
+// Organisation: work items of (sequence, kv head, 256 rows), a row being a
 // (query token, query head of the kv head's group) pair, so the G heads that
 // share a kv head share every K/V tile.  The 256 rows are two tiles A and B of
-// 128 (TMEM lanes); every K/V tile staged in shared memory feeds both.  Twelve
-// warps (the third warpgroup hands most of its registers to the first two):
-//   warps 0-3  tile A, one thread per row: Q row to shared memory, the softmax
-//              of each S tile, the rescale of O, the epilogue;
+// 128 (TMEM lanes); every K/V tile staged in shared memory feeds both.  One
+// persistent CTA per SM takes items from a launch-wide counter in the planner's
+// order (longest sequences first); the K/V ring, the MMAs and the softmax run on
+// from one item into the next, so an item's first tiles overlap the previous
+// item's last ones and its epilogue.  Twelve warps (the third warpgroup hands
+// most of its registers to the first two):
+//   warps 0-3  tile A, one thread per row: the softmax of each S tile, the
+//              rescale of O, the epilogue;
 //   warps 4-7  the same for tile B;
-//   warp 8     TMA producer: K_0, V_0, K_1, V_1, ... into a 5-stage ring, one
-//              4-D box per (block, kv head) row of the pool;
+//   warp 8     takes the items; TMA producer: the item's Q rows, then K_0, V_0,
+//              K_1, V_1, ... into a 5-stage ring, one 4-D box per (block, kv
+//              head) row of the pool;
 //   warp 9     TMEM allocation; one lane issues the MMAs; warps 10-11 idle.
 // Per 128-token tile j and row tile X:  S_X = Q_X K_j^T (M 128, N 128, K 128;
 // Q from shared memory, S in TMEM), then O_X += P_X V_j (P in TMEM, written
@@ -57,9 +62,9 @@ constexpr int kOffBars = kOffRing + kStages * kTileBytes;
 constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
 constexpr int kThreads = 384;                         // 8 row warps; producer, MMA, 2 idle
 // registers per thread after the split: the row warpgroups take what the third
-// warpgroup gives back (216 x 256 + 64 x 128 <= 168 x 384, the launch's budget)
+// warpgroup gives back (216 x 256 + 72 x 128 = 168 x 384, the launch's budget)
 constexpr int kRowRegs = 216;
-constexpr int kAuxRegs = 64;
+constexpr int kAuxRegs = 72;
 // TMEM columns (lane = row): S_X (fp32) at 128 X, its first 64 columns reused
 // for P_X (16-bit, two per column); O_X (fp32) at 256 + 128 X
 constexpr uint32_t kTmemCols = 512;
@@ -71,13 +76,9 @@ static_assert(kMqRows == 2 * kTile, "a CTA holds two row tiles");
 static_assert(kRowRegs * 256 + kAuxRegs * 128 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "the register split fits the launch's registers");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1;
-static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM slot and flag fit their region");
-
-// 16-byte chunk c (0..7) of row r of a 128B-swizzled [rows x 128 B] region.
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-    return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
-}
+constexpr int kItemReaders = 9;                       // warps reading each item index
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1 + 2 + 2 + 2 + 1;
+static_assert(kNumBars * 8 + 16 <= 256, "barriers, TMEM slot, flag and item ring fit their region");
 
 template <typename QT>
 __device__ __forceinline__ uint32_t pack2(float a, float b, float& ra, float& rb) {
@@ -178,73 +179,183 @@ __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
         if (tid == blockDim.x - 1) carry += incl;
         __syncthreads();
     }
-    if (tid == 0) p.item_prefix[p.num_seqs] = carry;
+    if (tid == 0) {
+        p.item_prefix[p.num_seqs] = carry;
+        *p.work_next = 0;                        // the attention CTAs' item counter
+    }
 }
 
-// ---- the TMA producer warp: ring item 2j is K_j, item 2j + 1 is V_j ----
+// ---- one work item: a sequence, a kv head and a pair of 128-row tiles ----
+struct MqItem {
+    int s, kvh, q_begin, n, ctx, q0;
+    int qn_a, qn_b;                // query tokens of row tiles A and B (B may have none)
+    int kv_end_a, kv_end_b;        // tokens [0, kv_end_X) are read for tile X
+    int T_a, T_b, T;               // 128-token K/V tiles of A, of B, of the item
+    int kv_end;                    // tokens the item stages
+};
+
+// Item `idx` in launch order: the last sequence (in launch order) whose first item
+// is <= idx, then its row pair (later, longer pairs first) and its kv head.
+__device__ __forceinline__ MqItem mq_item(const MqParams& p, int idx) {
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(&p.item_prefix[mid]) <= idx) lo = mid;
+        else hi = mid - 1;
+    }
+    MqItem it;
+    it.s = __ldg(&p.seq_order[lo]);
+    const int local = idx - __ldg(&p.item_prefix[lo]);
+    const int G = p.group, qpt = kTile / G;
+    it.q_begin = __ldg(&p.query_start[it.s]);
+    it.n = __ldg(&p.query_start[it.s + 1]) - it.q_begin;
+    it.ctx = __ldg(&p.context_lens[it.s]);
+    const int pairs = (it.n * G + kMqRows - 1) / kMqRows;
+    const int ct = pairs - 1 - local / p.num_kv_heads;
+    it.kvh = local % p.num_kv_heads;
+    it.q0 = 2 * ct * qpt;
+    it.qn_a = min(qpt, it.n - it.q0);
+    it.qn_b = max(0, min(qpt, it.n - it.q0 - qpt));
+    it.kv_end_a = it.ctx - it.n + it.q0 + it.qn_a;
+    it.kv_end_b = it.qn_b > 0 ? it.ctx - it.n + it.q0 + qpt + it.qn_b : 0;
+    it.T_a = (it.kv_end_a + kTile - 1) / kTile;
+    it.T_b = (it.kv_end_b + kTile - 1) / kTile;
+    it.T = max(it.T_a, it.T_b);
+    it.kv_end = max(it.kv_end_a, it.kv_end_b);
+    return it;
+}
+
+// The CTA's k-th item index (-1: none left), published by the producer warp in a
+// two-slot ring; each reading warp releases the slot with one arrival (lane 0).
+__device__ __forceinline__ int mq_take_item(const volatile int* items_s, uint64_t* item_full,
+                                            uint64_t* item_empty, int k, volatile int* abort_flag,
+                                            unsigned* status) {
+    const int slot = k & 1;
+    int idx = -1;
+    if (mbar_wait(&item_full[slot], (k >> 1) & 1)) {
+        idx = items_s[slot];
+    } else {
+        set_status(status, PKV_DEV_WAIT_TIMEOUT);
+        *abort_flag = 1;
+    }
+    __syncwarp(__activemask());
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&item_empty[slot]);
+    return idx;
+}
+
+// ---- the TMA producer warp: per item, ring entries 2j (K_j) and 2j + 1 (V_j) ----
 __device__ __forceinline__ void mq_producer(const MqParams& p, const CUtensorMap* tmK,
-                                            const CUtensorMap* tmV, uint8_t* smem,
-                                            uint64_t* full, uint64_t* empty,
-                                            volatile int* abort_flag, int s, int kvh, int kv_end,
-                                            int T) {
+                                            const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                                            uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                            uint64_t* q_full, uint64_t* q_free,
+                                            volatile int* items_s, uint64_t* item_full,
+                                            uint64_t* item_empty, volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         prefetch_tensormap(tmK);
         prefetch_tensormap(tmV);
+        prefetch_tensormap(tmQ);
     }
     const uint64_t policy = l2_evict_last_policy();   // other CTAs re-read K/V
+    const uint64_t q_policy = l2_evict_first_policy();   // each query row is read once
     const int B = p.block_size;
-    const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
-    const int nb_all = (kv_end + B - 1) / B;          // table entries this CTA reads
-    // block-table window: lane l holds entry wb + l (cur) and wb + 32 + l (nxt); the
-    // next window loads as soon as the current one is entered, so a tile's entries
-    // are in registers when its stage frees (a tile spans <= 16 entries)
-    int wb = 0;
-    int cur = lane < nb_all ? trow[lane] : 0;
-    int nxt = lane + 32 < nb_all ? trow[lane + 32] : 0;
-    for (int i = 0; i < 2 * T; ++i) {
-        const int j = i >> 1, st = i % kStages;
-        const bool isV = i & 1;
-        if (!mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1u)) {
-            set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
-            *abort_flag = 1;
-            break;
-        }
-        const int t0 = j * kTile, t1 = min(t0 + kTile, kv_end);
-        const int fb = t0 / B, nblk = (t1 - 1) / B - fb + 1;   // <= 128 / B <= 16
-        if (fb >= wb + 32) {                          // warp-uniform: enter the next window
-            wb += 32;
-            cur = nxt;
-            nxt = wb + 32 + lane < nb_all ? trow[wb + 32 + lane] : 0;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nblk * B) * 256u);
-        __syncwarp();
-        const int src = fb + lane - wb;               // fb - wb < 32, lane < nblk <= 16
-        int phys = __shfl_sync(0xffffffffu, cur, src & 31);
-        if (fb + nblk > wb + 32) {                    // warp-uniform: the tile straddles
-            const int hi = __shfl_sync(0xffffffffu, nxt, src & 31);
-            if (src >= 32) phys = hi;
-        }
-        if (lane < nblk) {
-            if (phys < 0 || phys >= p.num_blocks) {
-                if (!isV) set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
-                phys = 0;
+    const int total = __ldg(&p.item_prefix[p.num_seqs]);
+    uint32_t rbase = 0;                               // ring entries of earlier items
+    for (int k = 0;; ++k) {
+        // the next item, taken from the launch-wide counter once this warp has issued
+        // every load of the previous one: CTAs take items in launch order, longest
+        // first, about two tile pairs before they finish their current item
+        int idx = -1;
+        if (lane == 0) {
+            const int slot = k & 1;
+            if (!mbar_wait(&item_empty[slot], ((k >> 1) & 1) ^ 1u)) {
+                set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+            } else if (!*abort_flag) {
+                idx = atomicAdd(p.work_next, 1);
+                if (idx >= total) idx = -1;
             }
-            // one box per block: both 128-byte halves of its B rows, landing as
-            // [group of 8 rows][half][8 rows][128 B] at the block's place in the tile
-            const int y = (phys * p.num_kv_heads + kvh) * B;
-            uint8_t* dst = smem + kOffRing + st * kTileBytes + lane * B * 256;
-            tc5::tma_load_4d(dst, isV ? tmV : tmK, 0, 0, 0, y >> 3, &full[st], policy);
+            items_s[slot] = idx;
+            mbar_arrive(&item_full[slot]);
         }
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx < 0) break;
+        const MqItem it = mq_item(p, idx);
+        const int32_t* trow = p.block_tables + (int64_t)it.s * p.max_blocks;
+        const int nb_all = (it.kv_end + B - 1) / B;   // table entries this item reads
+        // block-table window: lane l holds entry wb + l (cur) and wb + 32 + l (nxt); the
+        // next window loads as soon as the current one is entered, so a tile's entries
+        // are in registers when its stage frees (a tile spans <= 16 entries)
+        int wb = 0;
+        int cur = lane < nb_all ? trow[lane] : 0;
+        int nxt = lane + 32 < nb_all ? trow[lane + 32] : 0;
+        bool ok = true;
+        for (int i = 0; i < 2 * it.T; ++i) {
+            if (i == 1 && lane == 0) {
+                // the item's Q rows, once the previous item's S MMAs no longer read Q
+                // (after its first K tile, so that K/V streaming starts first): per row
+                // tile with rows, two boxes of 64 elements x G heads x 128 / G tokens
+                if (k > 0 && !mbar_wait(q_free, (k - 1) & 1)) {
+                    set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                const int nx = it.qn_b > 0 ? 2 : 1, G = p.group;
+                mbar_arrive_expect_tx(q_full, (uint32_t)(nx * kTileBytes));
+                for (int X = 0; X < nx; ++X)
+                    for (int h = 0; h < 2; ++h)
+                        tc5::tma_load_3d(smem + kOffQ + X * kTileBytes + h * kHalfBytes, tmQ, 64 * h,
+                                         it.kvh * G, it.q_begin + it.q0 + X * (kTile / G), q_full,
+                                         q_policy);
+            }
+            const uint32_t g = rbase + (uint32_t)i;
+            const int j = i >> 1, st = (int)(g % kStages);
+            const bool isV = i & 1;
+            if (!mbar_wait(&empty[st], ((g / kStages) & 1) ^ 1u)) {
+                set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            const int t0 = j * kTile, t1 = min(t0 + kTile, it.kv_end);
+            const int fb = t0 / B, nblk = (t1 - 1) / B - fb + 1;   // <= 128 / B <= 16
+            if (fb >= wb + 32) {                          // warp-uniform: enter the next window
+                wb += 32;
+                cur = nxt;
+                nxt = wb + 32 + lane < nb_all ? trow[wb + 32 + lane] : 0;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)(nblk * B) * 256u);
+            __syncwarp();
+            const int src = fb + lane - wb;               // fb - wb < 32, lane < nblk <= 16
+            int phys = __shfl_sync(0xffffffffu, cur, src & 31);
+            if (fb + nblk > wb + 32) {                    // warp-uniform: the tile straddles
+                const int hi = __shfl_sync(0xffffffffu, nxt, src & 31);
+                if (src >= 32) phys = hi;
+            }
+            if (lane < nblk) {
+                if (phys < 0 || phys >= p.num_blocks) {
+                    if (!isV) set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    phys = 0;
+                }
+                // one box per block: both 128-byte halves of its B rows, landing as
+                // [group of 8 rows][half][8 rows][128 B] at the block's place in the tile
+                const int y = (phys * p.num_kv_heads + it.kvh) * B;
+                uint8_t* dst = smem + kOffRing + st * kTileBytes + lane * B * 256;
+                tc5::tma_load_4d(dst, isV ? tmV : tmK, 0, 0, 0, y >> 3, &full[st], policy);
+            }
+        }
+        if (!ok) break;
+        rbase += 2u * (uint32_t)it.T;
     }
 }
 
-// ---- the MMA issuer (one thread): PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) ----
+// ---- the MMA issuer (one thread): per item PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) ----
 template <typename QT>
-__device__ __forceinline__ void mq_mma(uint8_t* smem, uint32_t tmem, uint64_t* full,
-                                       uint64_t* empty, uint64_t* s_full, uint64_t* p_full,
-                                       uint64_t* q_full, uint64_t* drain, unsigned* status,
-                                       volatile int* abort_flag, int T, int T_a, int T_b) {
+__device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_t tmem,
+                                       uint64_t* full, uint64_t* empty, uint64_t* s_full,
+                                       uint64_t* p_full, uint64_t* q_full, uint64_t* q_free,
+                                       uint64_t* drain, uint64_t* o_free, uint64_t* fin,
+                                       const volatile int* items_s, uint64_t* item_full,
+                                       uint64_t* item_empty, volatile int* abort_flag) {
     constexpr bool kBF16 = std::is_same<QT, BF16>::value;
     constexpr uint32_t idqk = tc5::idesc_f16(kBF16, kTile, kTile, false, false);
     constexpr uint32_t idpv = tc5::idesc_f16(kBF16, kTile, kHD, false, true);
@@ -278,52 +389,69 @@ __device__ __forceinline__ void mq_mma(uint8_t* smem, uint32_t tmem, uint64_t* f
             tc5::mma_ts_w(d, a + (uint32_t)(8 * k), vx + (uint32_t)((k * 2 * kGroupBytes) >> 4), v_hi,
                           idpv, acc || k > 0);
     };
-    auto wait_item = [&](int i) {
-        const bool r = mbar_wait(&full[i % kStages], (i / kStages) & 1);
+    auto wait_entry = [&](uint32_t g) {
+        const bool r = mbar_wait(&full[g % kStages], (g / kStages) & 1);
         tc5::fence_after_sync();
         return r;
     };
-    auto wait_p = [&](int X, int j) {
-        const bool r = mbar_wait(&p_full[X], j & 1);
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+        const bool r = mbar_wait(bar, parity);
         tc5::fence_after_sync();
         return r;
     };
-    bool ok = mbar_wait(q_full, 0) && wait_item(0);
-    if (ok) {
-        issue_s(0, 0);
-        if (T_b > 0) issue_s(1, 0);
-        tc5::commit(&empty[0]);
-    }
-    for (int j = 0; j < T && ok; ++j) {
-        const int vs = (2 * j + 1) % kStages, ks = (2 * j + 2) % kStages;
-        const bool next = j + 1 < T;
-        if (!wait_item(2 * j + 1)) { ok = false; break; }
-        if (j < T_a) {
-            if (!wait_p(0, j)) { ok = false; break; }
-            issue_pv(0, vs, j > 0);
+    bool ok = true;
+    uint32_t rbase = 0, np_a = 0, np_b = 0;              // ring entries; P tiles consumed
+    for (int k = 0; ok; ++k) {
+        const int idx = mq_take_item(items_s, item_full, item_empty, k, abort_flag, p.status);
+        if (idx < 0 || *abort_flag) break;
+        const MqItem it = mq_item(p, idx);
+        if (!wait_bar(q_full, k & 1) || !wait_entry(rbase)) { ok = false; break; }
+        issue_s(0, (int)(rbase % kStages));
+        if (it.T_b > 0) issue_s(1, (int)(rbase % kStages));
+        tc5::commit(&empty[rbase % kStages]);
+        if (it.T == 1) tc5::commit(q_free);              // the item's last S MMAs
+        // the previous item's epilogue has read O_A and O_B before P.V overwrites them
+        if (k > 0 && (!wait_bar(&o_free[0], (k - 1) & 1) || !wait_bar(&o_free[1], (k - 1) & 1))) {
+            ok = false;
+            break;
         }
-        if (next && !wait_item(2 * j + 2)) { ok = false; break; }
-        if (j + 1 < T_a) issue_s(0, ks);
-        if (j < T_b) {
-            if (!wait_p(1, j)) { ok = false; break; }
-            issue_pv(1, vs, j > 0);
+        for (int j = 0; j < it.T && ok; ++j) {
+            const uint32_t gv = rbase + 2u * j + 1u, gk = gv + 1u;
+            const int vs = (int)(gv % kStages), ks = (int)(gk % kStages);
+            const bool next = j + 1 < it.T;
+            if (!wait_entry(gv)) { ok = false; break; }
+            if (j < it.T_a) {
+                if (!wait_bar(&p_full[0], np_a++ & 1)) { ok = false; break; }
+                issue_pv(0, vs, j > 0);
+            }
+            if (next && !wait_entry(gk)) { ok = false; break; }
+            if (j + 1 < it.T_a) issue_s(0, ks);
+            if (j < it.T_b) {
+                if (!wait_bar(&p_full[1], np_b++ & 1)) { ok = false; break; }
+                issue_pv(1, vs, j > 0);
+            }
+            tc5::commit(&empty[vs]);
+            if (j + 1 < it.T_b) issue_s(1, ks);
+            if (next) tc5::commit(&empty[ks]);
+            if (j == it.T - 2) tc5::commit(q_free);      // the item's last S MMAs: Q is free
         }
-        tc5::commit(&empty[vs]);
-        if (j + 1 < T_b) issue_s(1, ks);
-        if (next) tc5::commit(&empty[ks]);
+        // the item's O is complete once every MMA issued so far has completed
+        tc5::commit(drain);
+        rbase += 2u * (uint32_t)it.T;
     }
-    // every MMA issued above completes before O is read and the TMEM released
-    tc5::commit(drain);
-    if (!mbar_wait(drain, 0)) ok = false;
+    // every MMA issued above completes before the TMEM is released
+    tc5::commit(fin);
+    if (!mbar_wait(fin, 0)) ok = false;
     if (!ok) {
-        set_status(status, PKV_DEV_WAIT_TIMEOUT);
+        set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
         *abort_flag = 1;
     }
 }
 
 template <typename QT>
 __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
-    MqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    MqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    const __grid_constant__ CUtensorMap tmQ) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -332,42 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     uint64_t* empty = full + kStages;            // [kStages] the MMAs reading it completed
     uint64_t* s_full = empty + kStages;          // [2] S_X computed (and PV_X of the tile before)
     uint64_t* p_full = s_full + 2;               // [2] P_X written, O_X rescaled (128 arrivals)
-    uint64_t* q_full = p_full + 2;               // Q rows written (256 arrivals)
-    uint64_t* drain = q_full + 1;                // every MMA of the CTA completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* q_full = p_full + 2;               // an item's Q rows landed (TMA bytes)
+    uint64_t* q_free = q_full + 1;               // an item's S MMAs completed: Q may be replaced
+    uint64_t* drain = q_free + 1;                // an item's MMAs completed
+    uint64_t* o_free = drain + 1;                // [2] an item's O_X read by its epilogue (128)
+    uint64_t* item_full = o_free + 2;            // [2] an item index published
+    uint64_t* item_empty = item_full + 2;        // [2] read by the MMA and row warps
+    uint64_t* fin = item_empty + 2;              // every MMA of the CTA completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* items_s = abort_flag + 1;      // [2] the item ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- this CTA's item: in launch order, the last sequence whose first item is
-    // <= blockIdx.x ----
-    const int b = blockIdx.x;
-    if (b >= p.item_prefix[p.num_seqs]) return;   // whole CTA, before any allocation
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.item_prefix[mid] <= b) lo = mid;
-        else hi = mid - 1;
-    }
-    const int s = p.seq_order[lo];
-    const int local = b - p.item_prefix[lo];
-    const int G = p.group;
-    const int q_begin = p.query_start[s];
-    const int n = p.query_start[s + 1] - q_begin;
-    const int ctx = p.context_lens[s];
-    const int qpt = kTile / G;                            // query tokens per row tile
-    const int ctas = (n * G + kMqRows - 1) / kMqRows;
-    const int ct = ctas - 1 - local / p.num_kv_heads;     // later (longer) row pairs first
-    const int kvh = local % p.num_kv_heads;
-    // row tile X (A = 0, B = 1) covers queries [q0 + X qpt, .. + qn_X) and reads
-    // tokens [0, kv_end_X); tile A is never empty, tile B may be
-    const int q0 = 2 * ct * qpt;
-    const int qn_a = min(qpt, n - q0), qn_b = max(0, min(qpt, n - q0 - qpt));
-    const int kv_end_a = ctx - n + q0 + qn_a;
-    const int kv_end_b = qn_b > 0 ? ctx - n + q0 + qpt + qn_b : 0;
-    const int T_a = (kv_end_a + kTile - 1) / kTile, T_b = (kv_end_b + kTile - 1) / kTile;
-    const int kv_end = max(kv_end_a, kv_end_b);           // tokens the CTA stages
-    const int T = max(T_a, T_b);                          // K/V tiles; T_a >= 1
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -377,9 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kTile);
+            mbar_init(&o_free[i], kTile);
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], kItemReaders);
         }
-        mbar_init(q_full, 2 * kTile);
+        mbar_init(q_full, 1);
+        mbar_init(q_free, 1);
         mbar_init(drain, 1);
+        mbar_init(fin, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -392,11 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     if (warp >= 8) {
         tc5::setmaxnreg_dec<kAuxRegs>();
         if (warp == 8) {
-            mq_producer(p, &tmK, &tmV, smem, full, empty, abort_flag, s, kvh, kv_end, T);
+            mq_producer(p, &tmK, &tmV, &tmQ, smem, full, empty, q_full, q_free, items_s,
+                        item_full, item_empty, abort_flag);
         } else if (warp == 9) {
             if (lane == 0)
-                mq_mma<QT>(smem, tmem, full, empty, s_full, p_full, q_full, drain, p.status,
-                           abort_flag, T, T_a, T_b);
+                mq_mma<QT>(p, smem, tmem, full, empty, s_full, p_full, q_full, q_free, drain, o_free,
+                           fin, items_s, item_full, item_empty, abort_flag);
             __syncwarp();
         }
         // the TMEM is released once every thread is past its last use
@@ -414,157 +524,163 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         const int X = warp >> 2;
         const int r = threadIdx.x & (kTile - 1);          // TMEM lane = row
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const int Tx = X ? T_b : T_a, kv_end_r = X ? kv_end_b : kv_end_a;
-        const int qi = q0 + X * qpt + r / G, hq = kvh * G + r % G;
-        const bool row_valid = r < (X ? qn_b : qn_a) * G;
-        const int64_t qrow = ((int64_t)(q_begin + qi) * p.num_q_heads + hq) * kHD;
-        {
-            // the row's q into Q_X: [half][row][128 B], 16-byte chunks swizzled by row
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                              (row_valid ? qrow : 0));
-            uint8_t* qs = smem + kOffQ + X * kTileBytes;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalfBytes + sw128(r, c & 7)) = v;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(q_full);
-        }
-        // the V rows past the CTA's last token hold poison or stale data (0 x NaN would
-        // reach O through P = 0): the row tile whose P.V reads the last V tile first
-        // zeroes them once their copy has landed
-        const bool zeroes = (X == 0) == (T_a == T);
-        const int pos_r = ctx - n + qi;                   // this row's query position
         const uint32_t colS = tmem + lane_base + kColS + (uint32_t)(X * kTile),
                        colO = tmem + lane_base + kColO + (uint32_t)(X * kTile);
-        float m_run = -INFINITY, l_run = 0.f;
+        const int G = p.group, qpt = kTile / G;
         bool ok = true;
-        for (int j = 0; j < Tx; ++j) {
-            // wait decisions are warp-uniform: the tcgen05 loads and stores below need
-            // the whole warp converged
-            const bool got = !*abort_flag && mbar_wait(&s_full[X], j & 1);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            tc5::fence_after_sync();
-            // local tokens <= lim are visible (rows past the last query see no further);
-            // a tile every row of the warp sees whole needs no mask
-            const int lim = min(pos_r, kv_end_r - 1) - j * kTile;
-            const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1);
-            uint32_t sv[4][32];
+        uint32_t rbase = 0, ns = 0;                       // ring entries; S_X tiles seen
+        int idx = mq_take_item(items_s, item_full, item_empty, 0, abort_flag, p.status);
+        MqItem it{};
+        if (idx >= 0) it = mq_item(p, idx);
+        for (int k = 0; idx >= 0 && ok; ++k) {
+            const int Tx = X ? it.T_b : it.T_a;
+            const int qi = it.q0 + X * qpt + r / G;
+            const bool row_valid = r < (X ? it.qn_b : it.qn_a) * G;
+            const int64_t qrow = ((int64_t)(it.q_begin + qi) * p.num_q_heads + it.kvh * G + r % G) * kHD;
+            // the last token the row sees (rows past the last query see no further)
+            const int lim_row = min(it.ctx - it.n + qi, (X ? it.kv_end_b : it.kv_end_a) - 1);
+            // the V rows past the item's last token hold poison or stale data (0 x NaN
+            // would reach O through P = 0): the row tile whose P.V reads the last V tile
+            // first zeroes them once their copy has landed
+            const bool zeroes = (X == 0) == (it.T_a == it.T);
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int j = 0; j < Tx; ++j) {
+                // wait decisions are warp-uniform: the tcgen05 loads and stores below
+                // need the whole warp converged
+                const bool got = !*abort_flag && mbar_wait(&s_full[X], ns++ & 1);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                tc5::fence_after_sync();
+                // local tokens <= lim are visible; a tile every row of the warp sees whole
+                // needs no mask
+                const int lim = lim_row - j * kTile;
+                const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1);
+                uint32_t sv[4][32];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tc5::ld_32x32b_x32(colS + (uint32_t)(32 * c4), sv[c4]);
-            tc5::wait_ld();
-            if (masked) {
+                for (int c4 = 0; c4 < 4; ++c4) tc5::ld_32x32b_x32(colS + (uint32_t)(32 * c4), sv[c4]);
+                tc5::wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int c = 0; c < kTile; ++c)
+                        if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                }
+                // row max of the raw scores (the scale is positive: same order), with 8
+                // independent partial maxima
+                float pmx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pmx[i] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < kTile; ++c)
-                    if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
-            }
-            // row max of the raw scores (the scale is positive: same order), with 8
-            // independent partial maxima
-            float pmx[8];
+                    pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(sv[c >> 5][c & 31]));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) pmx[i] = -INFINITY;
+                for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
+                const float mx = pmx[0] * p.qk_scale_log2;
+                const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
+                const bool resc = j > 0 && m_new != m_run;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // PV_X(j-1) has completed (the commit of S_X(j) covers it)
+                    const float f = resc ? fast_exp2(m_run - m_new) : 1.f;
 #pragma unroll
-            for (int c = 0; c < kTile; ++c)
-                pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(sv[c >> 5][c & 31]));
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t o[32];
+                        tc5::ld_32x32b_x32(colO + (uint32_t)(c4 * 32), o);
+                        tc5::wait_ld();
 #pragma unroll
-            for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
-            const float mx = pmx[0] * p.qk_scale_log2;
-            const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
-            const bool resc = j > 0 && m_new != m_run;
-            if (__any_sync(0xffffffffu, resc)) {
-                // PV_X(j-1) has completed (the commit of S_X(j) covers it)
-                const float f = resc ? fast_exp2(m_run - m_new) : 1.f;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t o[32];
-                    tc5::ld_32x32b_x32(colO + (uint32_t)(c4 * 32), o);
-                    tc5::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tc5::st_32x32b_x32(colO + (uint32_t)(c4 * 32), o);
-                }
-                l_run *= f;
-            }
-            m_run = m_new;
-            // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
-            // operand type, over the first 64 columns of S_X; l sums the weights
-            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-            float pls[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) pls[i] = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pw[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = 64 * hh + 2 * e;
-                    const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
-                                                   p.qk_scale_log2, neg_m));
-                    const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
-                                                    p.qk_scale_log2, neg_m));
-                    pw[e] = pack2_bits<QT>(a, bb);
-                    pls[(2 * e) & 7] += a;
-                    pls[(2 * e + 1) & 7] += bb;
-                }
-                tc5::st_32x32b_x32(colS + (uint32_t)(32 * hh), pw);
-            }
-            float lsum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) lsum += pls[i];
-            l_run += lsum;
-            if (zeroes && j == T - 1 && kv_end - j * kTile < kTile) {
-                const int iv = 2 * j + 1;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&full[iv % kStages], (iv / kStages) & 1))) {
-                    ok = false;
-                    break;
-                }
-                if (r >= kv_end - j * kTile) {
-                    uint8_t* vrow = smem + kOffRing + (iv % kStages) * kTileBytes +
-                                    (r >> 3) * kGroupBytes + (r & 7) * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        *reinterpret_cast<uint4*>(vrow + kGroupHalf + c * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tc5::st_32x32b_x32(colO + (uint32_t)(c4 * 32), o);
                     }
+                    l_run *= f;
                 }
-                fence_proxy_async_smem();
+                m_run = m_new;
+                // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
+                // operand type, over the first 64 columns of S_X; l sums the weights
+                const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+                float pls[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pls[i] = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pw[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int c = 64 * hh + 2 * e;
+                        const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
+                                                       p.qk_scale_log2, neg_m));
+                        const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
+                                                        p.qk_scale_log2, neg_m));
+                        pw[e] = pack2_bits<QT>(a, bb);
+                        pls[(2 * e) & 7] += a;
+                        pls[(2 * e + 1) & 7] += bb;
+                    }
+                    tc5::st_32x32b_x32(colS + (uint32_t)(32 * hh), pw);
+                }
+                float lsum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lsum += pls[i];
+                l_run += lsum;
+                if (zeroes && j == it.T - 1 && it.kv_end - j * kTile < kTile) {
+                    const uint32_t gv = rbase + 2u * j + 1u;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&full[gv % kStages], (gv / kStages) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (r >= it.kv_end - j * kTile) {
+                        uint8_t* vrow = smem + kOffRing + (gv % kStages) * kTileBytes +
+                                        (r >> 3) * kGroupBytes + (r & 7) * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(vrow + kGroupHalf + c * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc5::wait_st();
+                tc5::fence_before_sync();
+                mbar_arrive(&p_full[X]);
             }
-            tc5::wait_st();
+            if (!ok) break;
+            rbase += 2u * (uint32_t)it.T;
+            // the next item (its Q arrives by TMA: the MMAs of the next item may start
+            // while this one's epilogue runs)
+            idx = mq_take_item(items_s, item_full, item_empty, k + 1, abort_flag, p.status);
+            MqItem nx{};
+            if (idx >= 0) nx = mq_item(p, idx);
+            // epilogue: every MMA of this item has completed (every thread waits, so the
+            // drain barrier's phases stay in step with the items)
+            ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(drain, k & 1));
+            if (!ok) break;
+            tc5::fence_after_sync();
+            uint32_t ov[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) tc5::ld_32x32b_x32(colO + (uint32_t)(c4 * 32), ov[c4]);
+            tc5::wait_ld();
             tc5::fence_before_sync();
-            mbar_arrive(&p_full[X]);
-        }
-        if (Tx > 0) {
-            if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(drain, 0));
-            if (ok) {
-                tc5::fence_after_sync();
+            mbar_arrive(&o_free[X]);                      // the next item's P.V may overwrite O_X
+            if (Tx > 0 && row_valid) {
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t o[32];
-                    tc5::ld_32x32b_x32(colO + (uint32_t)(c4 * 32), o);
-                    tc5::wait_ld();
-                    if (row_valid) {
-                        uint32_t w[16];
+                    uint32_t w[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            float ra, rb;
-                            w[e] = pack2<QT>(__uint_as_float(o[2 * e]) * inv,
-                                             __uint_as_float(o[2 * e + 1]) * inv, ra, rb);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                              qrow + c4 * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    for (int e = 0; e < 16; ++e) {
+                        float ra, rb;
+                        w[e] = pack2<QT>(__uint_as_float(ov[c4][2 * e]) * inv,
+                                         __uint_as_float(ov[c4][2 * e + 1]) * inv, ra, rb);
                     }
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow +
+                                                          c4 * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                 }
-            } else {
-                set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
-                *abort_flag = 1;
             }
+            it = nx;
+        }
+        if (!ok) {
+            set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+            *abort_flag = 1;
         }
     }
     tc5::fence_before_sync();
@@ -572,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
 }
 
 template <typename QT>
-cudaError_t launch_typed(const MqParams& p, int64_t max_items, cudaStream_t stream) {
+cudaError_t launch_typed(const MqParams& p, int64_t max_items, int num_ctas, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -586,13 +702,16 @@ cudaError_t launch_typed(const MqParams& p, int64_t max_items, cudaStream_t stre
     }
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    CUtensorMap tq;
     if (!encode_pool_map_grouped(&tk, p.k_cache, rows, p.block_size) ||
-        !encode_pool_map_grouped(&tv, p.v_cache, rows, p.block_size))
+        !encode_pool_map_grouped(&tv, p.v_cache, rows, p.block_size) ||
+        !encode_q_map(&tq, p.q, p.total_q, p.num_q_heads, p.group))
         return cudaErrorInvalidValue;
     mq_plan_kernel<<<1, 1024, 0, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    kernel<<<(unsigned)max_items, kThreads, kSmem, stream>>>(p, tk, tv);
+    const unsigned grid = (unsigned)(max_items < num_ctas ? max_items : (int64_t)num_ctas);
+    kernel<<<grid, kThreads, kSmem, stream>>>(p, tk, tv, tq);
     return cudaGetLastError();
 }
 
@@ -603,12 +722,12 @@ int64_t mq_max_items(int num_seqs, int total_q, int group, int num_kv_heads) {
 }
 
 cudaError_t launch_mq_attention(const MqParams& p, pkv_dtype q_dtype, int64_t max_items,
-                                cudaStream_t stream) {
+                                int num_sms, cudaStream_t stream) {
     if (max_items <= 0) return cudaSuccess;
-    if (max_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (max_items > 0x7fffffffLL || num_sms <= 0) return cudaErrorInvalidValue;
     switch (q_dtype) {
-    case PKV_F16: return launch_typed<F16>(p, max_items, stream);
-    case PKV_BF16: return launch_typed<BF16>(p, max_items, stream);
+    case PKV_F16: return launch_typed<F16>(p, max_items, num_sms, stream);
+    case PKV_BF16: return launch_typed<BF16>(p, max_items, num_sms, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -19,6 +19,7 @@ struct MqParams {
     void* out;                     // [total_q, Hq, d]
     int* item_prefix;              // workspace [S + 1]: items before the k-th launched sequence
     int* seq_order;                // workspace [S]: the sequence launched k-th
+    int* work_next;                // workspace: the next item a CTA takes
     unsigned* status;
     int num_seqs, total_q, num_q_heads, num_kv_heads, group, head_dim, block_size, num_blocks;
     int max_blocks;
@@ -26,10 +27,11 @@ struct MqParams {
     float qk_scale_log2;           // scale * log2(e)
 };
 
-// Upper bound of the CTAs the launch needs (items of every sequence).
+// Upper bound of the work items of a launch (items of every sequence).
 int64_t mq_max_items(int num_seqs, int total_q, int group, int num_kv_heads);
 
+// Launches the planner and min(max_items, num_sms) persistent attention CTAs.
 cudaError_t launch_mq_attention(const MqParams& p, pkv_dtype q_dtype, int64_t max_items,
-                                cudaStream_t stream);
+                                int num_sms, cudaStream_t stream);
 
 }  // namespace pkv

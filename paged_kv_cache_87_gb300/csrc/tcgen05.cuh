@@ -131,6 +131,19 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
         ::"r"(smem_addr(bar)) : "memory");
 }
 
+// ---------------------------------------------------------------- TMA 3-D --
+
+// 3-D TMA tile load global -> shared, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0,
+                                            int c1, int c2, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(c2), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- TMA 4-D --
 
 // 4-D TMA tile load global -> shared, completing on `bar`.

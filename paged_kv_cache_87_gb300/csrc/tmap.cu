@@ -67,4 +67,22 @@ bool encode_pool_map_grouped(CUtensorMap* map, const void* pool, long long rows,
            CUDA_SUCCESS;
 }
 
+bool encode_q_map(CUtensorMap* map, const void* q, long long total_q, int num_q_heads, int group) {
+    EncodeTiled enc = encoder();
+    if (!enc || total_q <= 0 || total_q > 0x7fffffffLL || num_q_heads <= 0 || group <= 0 ||
+        128 % group != 0 || num_q_heads % group != 0)
+        return false;
+    // [total_q][num_q_heads][128] 16-bit elements as (element, head, token); a box of
+    // 64 elements x group heads x 128 / group tokens lands as 128 rows of 128 bytes,
+    // row = token * group + head, 128-byte swizzled; rows past total_q read zeros
+    const cuuint64_t dims[3] = {128, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)num_q_heads * 256};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace pkv

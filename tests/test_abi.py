@@ -116,8 +116,8 @@ def test_multi_query_host_validation(lib):
     assert _multi_query(lib) == E.PKV_ERR_WORKSPACE
     assert _multi_query(lib, ws=4096, wsb=8) == E.PKV_ERR_WORKSPACE
     assert _multi_query(lib, tq=0, query=None) == E.PKV_OK           # nothing to do
-    assert binding.pkv_multi_query_workspace_bytes(4) == 512         # item prefix + launch order
-    assert binding.pkv_multi_query_workspace_bytes(1000) == 8192
+    assert binding.pkv_multi_query_workspace_bytes(4) == 768   # item prefix, launch order, counter
+    assert binding.pkv_multi_query_workspace_bytes(1000) == 8448
 
 
 def test_reshape_and_copy_host_validation(lib):
