@@ -106,6 +106,30 @@ __device__ __forceinline__ uint32_t pack2_bits(float a, float b) {
     }
 }
 
+// Packed fp32 pairs (sm_100 family): one instruction for two lanes of work.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float f2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
+__device__ __forceinline__ float f2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
+// x * s + m, element-wise, rounded once (as fmaf)
+__device__ __forceinline__ uint64_t f2_fma(uint64_t x, uint64_t s, uint64_t m) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(s), "l"(m));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// max of three (no NaN among the scores: masked ones are -inf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Items: per sequence ceil(n * G / 256) row pairs times Hkv, the sequences taken
 // longest context first (up to kMqSortSeqs sequences; beyond, in index order) so
 // that the block scheduler hands out the longest CTAs first; exclusive prefix.
@@ -563,17 +587,16 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     for (int c = 0; c < kTile; ++c)
                         if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
                 }
-                // row max of the raw scores (the scale is positive: same order), with 8
-                // independent partial maxima
-                float pmx[8];
+                // row max of the raw scores (the scale is positive: same order): four
+                // independent partial maxima, two scores per three-input max
+                float pmx[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pmx[i] = -INFINITY;
+                for (int i = 0; i < 4; ++i) pmx[i] = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < kTile; ++c)
-                    pmx[c & 7] = fmaxf(pmx[c & 7], __uint_as_float(sv[c >> 5][c & 31]));
-#pragma unroll
-                for (int i = 1; i < 8; ++i) pmx[0] = fmaxf(pmx[0], pmx[i]);
-                const float mx = pmx[0] * p.qk_scale_log2;
+                for (int c = 0; c < kTile; c += 2)
+                    pmx[(c >> 1) & 3] = max3(pmx[(c >> 1) & 3], __uint_as_float(sv[c >> 5][c & 31]),
+                                             __uint_as_float(sv[c >> 5][(c + 1) & 31]));
+                const float mx = max3(pmx[0], pmx[1], fmaxf(pmx[2], pmx[3])) * p.qk_scale_log2;
                 const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
                 const bool resc = j > 0 && m_new != m_run;
                 if (__any_sync(0xffffffffu, resc)) {
@@ -591,32 +614,32 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                     l_run *= f;
                 }
                 m_run = m_new;
-                // P = 2^(scale * s - m) (one FMA and one ex2 per score), rounded to the
-                // operand type, over the first 64 columns of S_X; l sums the weights
+                // P = 2^(scale * s - m) (one FMA and one ex2 per score; the FMAs and the
+                // sums two scores per packed instruction), rounded to the operand type,
+                // over the first 64 columns of S_X; l sums the weights
                 const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-                float pls[8];
+                const uint64_t scale2 = f2_pack(p.qk_scale_log2, p.qk_scale_log2),
+                               negm2 = f2_pack(neg_m, neg_m);
+                uint64_t pls[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pls[i] = 0.f;
+                for (int i = 0; i < 4; ++i) pls[i] = 0ull;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pw[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int c = 64 * hh + 2 * e;
-                        const float a = fast_exp2(fmaf(__uint_as_float(sv[c >> 5][c & 31]),
-                                                       p.qk_scale_log2, neg_m));
-                        const float bb = fast_exp2(fmaf(__uint_as_float(sv[(c + 1) >> 5][(c + 1) & 31]),
-                                                        p.qk_scale_log2, neg_m));
+                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[c >> 5][c & 31]),
+                                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])),
+                                                  scale2, negm2);
+                        const float a = fast_exp2(f2_lo(x)), bb = fast_exp2(f2_hi(x));
                         pw[e] = pack2_bits<QT>(a, bb);
-                        pls[(2 * e) & 7] += a;
-                        pls[(2 * e + 1) & 7] += bb;
+                        pls[e & 3] = f2_add(pls[e & 3], f2_pack(a, bb));
                     }
                     tc5::st_32x32b_x32(colS + (uint32_t)(32 * hh), pw);
                 }
-                float lsum = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) lsum += pls[i];
-                l_run += lsum;
+                const uint64_t l2 = f2_add(f2_add(pls[0], pls[1]), f2_add(pls[2], pls[3]));
+                l_run += f2_lo(l2) + f2_hi(l2);
                 if (zeroes && j == it.T - 1 && it.kv_end - j * kTile < kTile) {
                     const uint32_t gv = rbase + 2u * j + 1u;
                     if (!__all_sync(0xffffffffu,
