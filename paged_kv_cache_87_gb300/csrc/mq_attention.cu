@@ -59,7 +59,7 @@ constexpr int kStages = 5;                            // K/V ring: K_0, V_0, K_1
 constexpr int kOffQ = 0;                              // Q_A, Q_B: [half][128 rows][128 B]
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;
 constexpr int kOffBars = kOffRing + kStages * kTileBytes;
-constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag; alignment
+constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag, item ring; alignment
 constexpr int kThreads = 384;                         // 8 row warps; producer, MMA, 2 idle
 // registers per thread after the split: the row warpgroups take what the third
 // warpgroup gives back (216 x 256 + 72 x 128 = 168 x 384, the launch's budget)
@@ -123,7 +123,7 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-// max of three (no NaN among the scores: masked ones are -inf)
+// max of three (a NaN operand is ignored, as by fmaxf)
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -132,7 +132,8 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // Items: per sequence ceil(n * G / 256) row pairs times Hkv, the sequences taken
 // longest context first (up to kMqSortSeqs sequences; beyond, in index order) so
-// that the block scheduler hands out the longest CTAs first; exclusive prefix.
+// that the persistent CTAs take the longest items first; exclusive prefix.  The
+// CTAs' item counter starts at zero.
 constexpr int kMqSortSeqs = 1024;
 
 __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
