@@ -80,6 +80,10 @@ def _load():
                                                        i32, i32, i32, f64, i32, i32, f64, P,
                                                        i32, P, i32]
         lib.oracle_paged_prefill_attention.restype = i32
+        lib.oracle_paged_tree_attention.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                    i32, i32, i32, f64, i32, i32, f64, P,
+                                                    i32, P, i32]
+        lib.oracle_paged_tree_attention.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -221,6 +225,43 @@ def paged_prefill_attention(query, k_cache, v_cache, block_tables, context_lens,
     if rc != 0:
         raise ValueError("oracle paged_prefill_attention: bad argument, more queries than "
                          "context, or block id out of range")
+    return out.reshape(total_q, num_q_heads, head_dim) if full else out
+
+
+def paged_tree_attention(query, k_cache, v_cache, block_tables, context_lens, query_start, tree,
+                         *, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, q_dtype, kv_dtype, kv_scale=1.0, sel=None,
+                         nthreads=1) -> np.ndarray:
+    """fp64 outputs of the verification of draft-token trees for the (query row, q head)
+    pairs in ``sel``.
+
+    The last n_s <= 64 tokens of sequence s are its tree, each after its ancestors;
+    query i sees the prior context, itself, and each earlier tree token j whose bit j
+    is set in tree[query_start[s] + i] (uint64).  Returns [len(sel), head_dim], or
+    [total_q, Hq, d] when ``sel`` is None.
+    """
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    context_lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    query_start = np.ascontiguousarray(query_start, dtype=np.int32)
+    tree = np.ascontiguousarray(tree, dtype=np.uint64)
+    S = context_lens.shape[0]
+    total_q = int(query_start[-1])
+    if tree.shape != (total_q,):
+        raise ValueError("tree: one uint64 per query row")
+    full = sel is None
+    if full:
+        sel = np.stack(np.meshgrid(np.arange(total_q), np.arange(num_q_heads), indexing="ij"),
+                       -1).reshape(-1, 2)
+    sel = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 2)
+    out = np.zeros((sel.shape[0], head_dim), dtype=np.float64)
+    rc = _load().oracle_paged_tree_attention(
+        _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start), _ptr(tree), S, num_q_heads, num_kv_heads, head_dim, block_size,
+        num_blocks, int(block_tables.shape[1]), float(scale), _code(q_dtype), _code(kv_dtype),
+        float(kv_scale), _ptr(sel), int(sel.shape[0]), _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle paged_tree_attention: bad argument, a tree of more than 64 "
+                         "tokens, more queries than context, or block id out of range")
     return out.reshape(total_q, num_q_heads, head_dim) if full else out
 
 

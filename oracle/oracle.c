@@ -404,6 +404,81 @@ int oracle_paged_prefill_attention(const void* query, const void* k_cache, const
     return bad ? -1 : 0;
 }
 
+/*
+ * Verification of a tree of draft tokens (speculative decoding trees, [P1] §9):
+ * the last n_s <= 64 tokens of sequence s are the tree's tokens, laid out so that
+ * every token comes after its ancestors.  Query i of the sequence sees every
+ * token of the prior context (positions < c0 = ctx - n_s), itself (position
+ * c0 + i), and each earlier tree token j < i whose bit j is set in
+ * tree[query_start[s] + i] (its ancestors); bits j >= i are ignored.  With
+ * bits 0 .. i-1 set this is the causal attention above.  The output is the
+ * softmax-weighted sum over exactly that set of tokens ([P1] §3), in fp64.
+ */
+int oracle_paged_tree_attention(const void* query, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                const int32_t* query_start, const uint64_t* tree, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, int max_blocks, double scale, int q_dtype,
+                                int kv_dtype, double kv_scale, const int32_t* sel, int num_sel,
+                                double* out, int nthreads) {
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || num_seqs < 0 || !tree) return -1;
+    if (!elem_bytes(q_dtype) || q_dtype == OR_E4M3 || !elem_bytes(kv_dtype)) return -1;
+    dec_args a;
+    fill_args(&a, query, k_cache, v_cache, block_tables, context_lens, num_q_heads,
+              num_kv_heads, head_dim, block_size, num_blocks, max_blocks, scale, q_dtype,
+              kv_dtype, kv_scale);
+    int bad = 0;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1) reduction(| : bad)
+    for (int k = 0; k < num_sel; ++k) {
+        int row = sel[2 * k], h = sel[2 * k + 1];
+        double* o = out + (int64_t)k * head_dim;
+        int s = -1;
+        for (int j = 0; j < num_seqs; ++j)
+            if (query_start[j] <= row && row < query_start[j + 1]) { s = j; break; }
+        if (s < 0) { bad = 1; continue; }
+        int n = query_start[s + 1] - query_start[s];
+        int ctx = context_lens[s];
+        if (n > 64 || n > ctx || ctx > max_blocks * block_size) { bad = 1; continue; }
+        int c0 = ctx - n, i = row - query_start[s];
+        uint64_t bits = tree[row];
+        /* the visible positions: the prior context, then ancestors and the token itself */
+        int* pos = malloc(sizeof(int) * (size_t)(c0 + i + 1));
+        int np = 0;
+        for (int t = 0; t < c0; ++t) pos[np++] = t;
+        for (int j = 0; j < i; ++j)
+            if ((bits >> j) & 1u) pos[np++] = c0 + j;
+        pos[np++] = c0 + i;
+        /* softmax over the visible logits, the weighted sum of their values */
+        int d = head_dim, g = h / (num_q_heads / num_kv_heads), rc = 0;
+        double* q = malloc(sizeof(double) * d);
+        double* krow = malloc(sizeof(double) * d);
+        double* z = malloc(sizeof(double) * np);
+        for (int e = 0; e < d; ++e)
+            q[e] = load_elem(a.query, a.q_dtype, ((int64_t)row * num_q_heads + h) * d + e);
+        double m = -INFINITY;
+        for (int u = 0; u < np && !rc; ++u) {
+            rc = fetch_row(&a, a.k_cache, s, g, pos[u], krow);
+            double dot = 0.0;
+            for (int e = 0; e < d; ++e) dot += q[e] * krow[e];
+            z[u] = a.scale * dot;
+            if (z[u] > m) m = z[u];
+        }
+        double l = 0.0;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        for (int u = 0; u < np && !rc; ++u) {
+            double w = exp(z[u] - m);
+            l += w;
+            rc = fetch_row(&a, a.v_cache, s, g, pos[u], krow);
+            for (int e = 0; e < d; ++e) o[e] += w * krow[e];
+        }
+        for (int e = 0; e < d; ++e) o[e] /= l;
+        free(pos); free(q); free(krow); free(z);
+        if (rc) bad = 1;
+    }
+    return bad ? -1 : 0;
+}
+
 /* Threads the OpenMP runtime would give a parallel region (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

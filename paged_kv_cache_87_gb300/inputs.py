@@ -428,6 +428,9 @@ class MultiQueryWorkload:
     context_lens: np.ndarray   # int32 [S] = prior + n
     query_start: np.ndarray    # int32 [S + 1]
     seq_tokens: list           # per sequence: its rows in position order
+    # draft-token trees: uint64 [total_q], bit j of row query_start[s] + i set when query
+    # i of sequence s sees tree token j < i (its ancestors); None for causal attention
+    tree: np.ndarray | None = None
 
     src_dtype = property(lambda self: self.kv_dtype)
     kv_scale = property(lambda self: 1.0)
@@ -454,10 +457,15 @@ class MultiQueryWorkload:
 
     @property
     def flops(self) -> int:
-        """Causal attention FLOPs: 4 d Hq per (query, visible key) pair (Q K^T and P V)."""
+        """Attention FLOPs: 4 d Hq per (query, visible key) pair (Q K^T and P V)."""
         n = self.num_new
         prior = self.context_lens.astype(np.int64) - n
-        pairs = int((n * prior + n * (n + 1) // 2).sum())
+        if self.tree is None:
+            pairs = int((n * prior + n * (n + 1) // 2).sum())
+        else:
+            # prior context + the token itself + its ancestors
+            anc = int(sum(bin(int(x)).count("1") for x in self.tree))
+            pairs = int((n * prior + n).sum()) + anc
         return 4 * self.head_dim * self.num_q_heads * pairs
 
     @property
@@ -503,10 +511,56 @@ def make_multi_query(name: str, rng: np.random.Generator, prior, n, *, num_q_hea
         seq_tokens=[np.arange(offsets[s], offsets[s + 1]) for s in range(S)])
 
 
+def tree_ancestors(parent) -> np.ndarray:
+    """uint64 ancestor masks of a tree given by parent indices (parent[0] = -1 for the
+    root, parent[i] < i otherwise): bit j of entry i set when j is an ancestor of i."""
+    parent = np.asarray(parent, dtype=np.int64)
+    n = parent.shape[0]
+    if n > 64:
+        raise ValueError("a tree of at most 64 tokens")
+    anc = np.zeros(n, dtype=np.uint64)
+    for i in range(1, n):
+        p = int(parent[i])
+        if not 0 <= p < i:
+            raise ValueError("parents precede their children")
+        anc[i] = anc[p] | np.uint64(1 << p)
+    return anc
+
+
+def random_tree_parents(rng: np.random.Generator, n: int, kind: str = "random") -> np.ndarray:
+    """Parent indices of an n-token draft tree laid out parents first: "chain" (each
+    token the child of the previous one), "star" (every token a child of the root) or
+    "random" (each token the child of one of the 4 tokens before it, so that branches
+    and depth both occur)."""
+    parent = np.full(n, -1, dtype=np.int64)
+    for i in range(1, n):
+        if kind == "chain":
+            parent[i] = i - 1
+        elif kind == "star":
+            parent[i] = 0
+        else:
+            parent[i] = int(rng.integers(max(0, i - 4), i))
+    return parent
+
+
+def make_tree_verify(name: str, rng: np.random.Generator, prior, n, *, kinds=None,
+                     **kw) -> MultiQueryWorkload:
+    """A multi-query workload whose queries are draft-token trees (n[s] <= 64 tokens each,
+    the tree of kind kinds[s], "random" by default) over prior[s] cached tokens."""
+    w = make_multi_query(name, rng, prior, n, **kw)
+    trees = []
+    for s in range(w.num_seqs):
+        kind = kinds[s] if kinds is not None else "random"
+        trees.append(tree_ancestors(random_tree_parents(rng, int(w.num_new[s]), kind)))
+    w.tree = np.concatenate(trees) if trees else np.zeros(0, np.uint64)
+    return w
+
+
 MQ_CONFIG_NAMES = {
     0: "multi-query mix: 5 seqs, 8q/2kv heads, d128, bf16, B16, prior {0..300} + 1..200 queries",
     1: "chunked prefill: 16 seqs, 32q/8kv heads, d128, bf16, B16, prior U[0,8192] + 512 queries",
     2: "prefill MHA: 4 seqs, 16 heads, d128, fp16, B16, prompts U[1024,4096], no prior context",
+    3: "draft-tree verification: 64 seqs, 32q/8kv heads, d128, bf16, B16, prior U[1024,8192] + trees of 64 tokens",
 }
 
 
@@ -525,6 +579,9 @@ def make_multi_query_config(cid: int, *, seed: int | None = None) -> MultiQueryW
         n = rng.integers(1024, 4096 + 1, size=4)
         return make_multi_query(name, rng, np.zeros(4, np.int64), n, num_q_heads=16,
                                 num_kv_heads=16, dtype="f16")
+    if cid == 3:
+        prior = rng.integers(1024, 8192 + 1, size=64)
+        return make_tree_verify(name, rng, prior, np.full(64, 64), num_q_heads=32, num_kv_heads=8)
     raise ValueError(f"no multi-query workload {cid}")
 
 
