@@ -56,7 +56,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--multi-query", type=int, default=None, metavar="ID",
                     help="measure the multi-query (causal) paged attention on multi-query "
-                         "workload ID (1: chunked prefill) instead of the decode")
+                         "workload ID (1: chunked prefill, 2: prefill, 3: draft-tree "
+                         "verification) instead of the decode")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="store the DRAM bytes per decode launch of an ncu --csv capture "
                          "(dram__bytes_read.sum, dram__bytes_write.sum of decode_mma / "
@@ -454,6 +455,32 @@ def measured_tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def mq_roofline(w, sec_att: float) -> dict:
+    """Roofline of the multi-query attention launch: tensor-bound (TFLOP/s against the
+    measured bf16 peak) when the workload's FLOPs per algorithmic byte (every cached K/V
+    row once, the queries in, the outputs out) reach the ridge point of the measured
+    peaks, HBM-bound (GB/s against the measured copy bandwidth) below it."""
+    from paged_kv_cache_87_gb300.inputs import DTYPE_BYTES
+    tpeak, tsrc = measured_tensor_peak()
+    hpeak, hsrc = measured_peak()
+    io_bytes = w.kv_bytes + 2 * w.total_q * w.num_q_heads * w.head_dim * DTYPE_BYTES[w.q_dtype]
+    tflops = w.flops / sec_att / 1e12
+    gbs = io_bytes / sec_att / 1e9
+    intensity = w.flops / io_bytes
+    ridge = tpeak * 1e12 / (hpeak * 1e9)
+    r = {"flops_per_byte": round(intensity, 1), "ridge_flops_per_byte": round(ridge, 1),
+         "algorithmic_bytes": io_bytes}
+    if intensity >= ridge:
+        r.update(bound="tensor", achieved=round(tflops, 1), peak=tpeak, peak_source=tsrc,
+                 unit="TFLOP/s", frac=round(tflops / tpeak, 4),
+                 hbm_frac=round(gbs / hpeak, 4))
+    else:
+        r.update(bound="hbm", achieved=round(gbs, 1), peak=hpeak, peak_source=hsrc,
+                 unit="GB/s", frac=round(gbs / hpeak, 4),
+                 tensor_frac=round(tflops / tpeak, 4), tflops=round(tflops, 1))
+    return r
+
+
 def mq_oracle_sample(w, target_s: float, nthreads: int, seed: int = 0, caches=None):
     """The oracle on sampled (query row, head) pairs; returns (TFLOP/s, s, flops, desc)."""
     import oracle
@@ -471,19 +498,31 @@ def mq_oracle_sample(w, target_s: float, nthreads: int, seed: int = 0, caches=No
     seq_of_row = np.repeat(np.arange(w.num_seqs), np.diff(w.query_start))
     pos = (w.context_lens[seq_of_row] - np.diff(w.query_start)[seq_of_row] +
            (np.arange(w.total_q) - w.query_start[seq_of_row]))
+    tree = getattr(w, "tree", None)
+    if tree is not None:
+        # visible keys of a draft-tree row: the prior context, itself, its ancestors
+        anc = np.array([bin(int(x)).count("1") for x in tree], dtype=np.int64)
+        prior = w.context_lens[seq_of_row] - np.diff(w.query_start)[seq_of_row]
+        visible = prior + 1 + anc
+    else:
+        visible = pos + 1
+    args = dict(num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                block_size=w.block_size, num_blocks=w.num_blocks, scale=w.scale,
+                q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, nthreads=nthreads)
 
     def run(k):
         rows = rng.integers(0, w.total_q, size=k)
         heads = rng.integers(0, w.num_q_heads, size=k)
         sel = np.stack([rows, heads], 1).astype(np.int32)
         t = time.perf_counter()
-        oracle.paged_prefill_attention(
-            w.query, kc, vc, w.block_tables, w.context_lens, w.query_start,
-            num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-            block_size=w.block_size, num_blocks=w.num_blocks, scale=w.scale, q_dtype=w.q_dtype,
-            kv_dtype=w.kv_dtype, sel=sel, nthreads=nthreads)
+        if tree is not None:
+            oracle.paged_tree_attention(w.query, kc, vc, w.block_tables, w.context_lens,
+                                        w.query_start, tree, sel=sel, **args)
+        else:
+            oracle.paged_prefill_attention(w.query, kc, vc, w.block_tables, w.context_lens,
+                                           w.query_start, sel=sel, **args)
         dt = time.perf_counter() - t
-        return dt, int(4 * w.head_dim * (pos[rows] + 1).sum())
+        return dt, int(4 * w.head_dim * visible[rows].sum())
 
     dt, fl = run(max(8, nthreads))                         # calibration
     k = int(max(8, nthreads) * max(1.0, target_s / max(dt, 1e-3)))
@@ -546,6 +585,8 @@ def run_mq(args, rank, world, local):
            (pin(torch.from_numpy(w.context_lens)), st.context_lens),
            (pin(torch.from_numpy(w.query_start)), st.query_start),
            (pin(torch.from_numpy(w.block_tables)), st.block_tables)]
+    if st.tree is not None:                                   # draft trees: their masks too
+        ins.append((pin(torch.from_numpy(w.tree.view(np.int64))), st.tree))
     h_out = pin(torch.empty_like(st.out, device="cpu"))
     h2d = sum(h.numel() * h.element_size() for h, _ in ins)
     d2h = h_out.numel() * h_out.element_size()
@@ -565,8 +606,7 @@ def run_mq(args, rank, world, local):
                 e2e_ms.append(a.elapsed_time(b))
     tot_e, slow_e, _ = aggregate(w.flops, float(np.mean(e2e_ms)) * 1e-3, world, device)
 
-    peak, peak_src = measured_tensor_peak()
-    achieved = w.flops / sec_att / 1e12
+    roof = mq_roofline(w, sec_att)
     traffic = recorded_traffic(f"mq{args.multi_query}")
     line = {
         "metric": MQ_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -580,9 +620,7 @@ def run_mq(args, rank, world, local):
                    "l2": "L2 flushed between steps (write of 2x L2)",
                    "step": "reshape_and_cache of the queries' tokens + multi-query attention",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                     "peak_source": peak_src, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
+        "roofline": {**roof, "traffic": traffic,
                      "kernel": "planning + attention kernels (CUDA events around the call)",
                      "attention_us": round(sec_att * 1e6, 2)},
         "e2e": {"value": round(tot_e / slow_e / 1e12, 2), "unit": "TFLOP/s",

@@ -214,6 +214,36 @@ PKV_API pkv_status pkv_paged_multi_query_attention(
     pkv_stream_t stream);
 
 /*
+ * Verification of draft-token trees (speculative decoding trees: "...Mathematical
+ * Foundations" §9 lists them among the uses of shared paged memory; the
+ * attention is that of §3).  As pkv_paged_multi_query_attention, except that
+ * the n_s <= 64 query tokens of sequence s are a tree of draft tokens, laid
+ * out so that every token comes after its ancestors, and query i of the
+ * sequence (row query_start[s] + i, position p = context_lens[s] - n_s + i)
+ * attends to
+ *   every token at a position < context_lens[s] - n_s (the prior context),
+ *   itself (position p), and
+ *   each tree token j < i whose bit j is set in tree_mask[query_start[s] + i]
+ *   (its ancestors); bits j >= i are ignored.
+ * With bits 0 .. i-1 set this is the causal attention of
+ * pkv_paged_multi_query_attention.
+ *
+ *   tree_mask    device uint64 [total_q], 8-byte aligned; not null unless
+ *                num_seqs or total_q is 0 (PKV_ERR_INVALID_ARG)
+ *   a sequence with more than 64 queries is skipped (its rows are left
+ *   untouched) and flagged PKV_DEV_BAD_CONTEXT.
+ * Workspace: pkv_multi_query_workspace_bytes(num_seqs).  Supported shapes and
+ * types, launches and the other arguments as pkv_paged_multi_query_attention.
+ */
+PKV_API pkv_status pkv_paged_tree_attention(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* query_start, const uint64_t* tree_mask,
+    int num_seqs, int total_q, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
+    pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
+    pkv_stream_t stream);
+
+/*
  * Write new tokens' keys and values into their cache slots
  * ("...Mathematical Foundations" §7 kernel 1; §4 Allocation Lifecycle step 2).
  *

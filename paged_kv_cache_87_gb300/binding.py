@@ -51,6 +51,12 @@ _SIGNATURES = {
                                                       ctypes.c_int, ctypes.c_float,
                                                       ctypes.c_void_p, ctypes.c_size_t,
                                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_paged_tree_attention": (
+        ctypes.c_int,
+        [ctypes.c_void_p] * 7 + [ctypes.c_int] * 9 + [ctypes.c_float, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_float,
+                                                      ctypes.c_void_p, ctypes.c_size_t,
+                                                      ctypes.c_void_p, ctypes.c_void_p]),
     "pkv_paged_decode_attention_noalloc": (
         ctypes.c_int,
         [ctypes.c_void_p] * 5 + [ctypes.c_int] * 8 + [ctypes.c_float, ctypes.c_int, ctypes.c_int,
@@ -222,6 +228,32 @@ def pkv_paged_multi_query_attention(query: torch.Tensor, k_cache: torch.Tensor,
     own (the last n_s).  Row i of sequence s attends to tokens
     0 .. context_lens[s] - n_s + i.
     """
+    return _multi_query("pkv_paged_multi_query_attention", query, k_cache, v_cache,
+                        block_tables, context_lens, query_start, None, max_context_len, scale,
+                        kv_scale, workspace, out, stream)
+
+
+def pkv_paged_tree_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             query_start: torch.Tensor, tree_mask: torch.Tensor,
+                             max_context_len: int, scale: float, kv_scale: float = 1.0,
+                             workspace: torch.Tensor | None = None,
+                             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Verification of draft-token trees: as pkv_paged_multi_query_attention, but the
+    n_s <= 64 queries of sequence s are a tree laid out parents first, and query i sees
+    the prior context, itself and each tree token j < i whose bit j is set in
+    tree_mask[query_start[s] + i] (int64 / uint64 bits, [total_q])."""
+    if tree_mask.dtype not in (torch.int64, torch.uint64) or tree_mask.dim() != 1 or \
+            int(tree_mask.shape[0]) != int(query.shape[0]):
+        raise ValueError("tree_mask must be 64-bit [total_q]")
+    _cuda(tree_mask, "tree_mask")
+    return _multi_query("pkv_paged_tree_attention", query, k_cache, v_cache, block_tables,
+                        context_lens, query_start, tree_mask, max_context_len, scale, kv_scale,
+                        workspace, out, stream)
+
+
+def _multi_query(name, query, k_cache, v_cache, block_tables, context_lens, query_start,
+                 tree_mask, max_context_len, scale, kv_scale, workspace, out, stream):
     total_q, Hq, d = query.shape
     NB, Hkv, B, d2 = k_cache.shape
     S = int(context_lens.shape[0])
@@ -243,13 +275,16 @@ def pkv_paged_multi_query_attention(query: torch.Tensor, k_cache: torch.Tensor,
         out = torch.empty_like(query)
     _cuda(out, "out")
     _cuda(workspace, "workspace")
-    st = load().pkv_paged_multi_query_attention(
-        query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), query_start.data_ptr(), S, total_q, Hq, Hkv, d, B, NB,
+    head = [query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), query_start.data_ptr()]
+    if tree_mask is not None:
+        head.append(tree_mask.data_ptr())
+    st = getattr(load(), name)(
+        *head, S, total_q, Hq, Hkv, d, B, NB,
         block_tables.shape[1], int(max_context_len), float(scale), dtype_code(query),
         dtype_code(k_cache), float(kv_scale), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
-    _check("pkv_paged_multi_query_attention", st)
+    _check(name, st)
     return out
 
 

@@ -378,10 +378,13 @@ size_t pkv_multi_query_workspace_bytes(int num_seqs) {
     return round_up(((size_t)num_seqs + 1) * 4, 256) + round_up((size_t)num_seqs * 4, 256) + 256;
 }
 
-pkv_status pkv_paged_multi_query_attention(
+namespace {
+
+// The multi-query entry points: causal (tree == nullptr) or draft-tree verification.
+pkv_status multi_query_attention(
     const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-    const int32_t* context_lens, const int32_t* query_start, int num_seqs, int total_q,
-    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    const int32_t* context_lens, const int32_t* query_start, const uint64_t* tree, int num_seqs,
+    int total_q, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
     int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
     pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
     pkv_stream_t stream) {
@@ -403,7 +406,7 @@ pkv_status pkv_paged_multi_query_attention(
         return PKV_ERR_INVALID_ARG;
     if (!aligned(query, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(out, 16) || !aligned(block_tables, 4) || !aligned(context_lens, 4) ||
-        !aligned(query_start, 4))
+        !aligned(query_start, 4) || !aligned(tree, 8))
         return PKV_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) ||
         workspace_bytes < pkv_multi_query_workspace_bytes(num_seqs))
@@ -417,6 +420,7 @@ pkv_status pkv_paged_multi_query_attention(
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.query_start = query_start;
+    p.tree = tree;
     p.out = out;
     p.item_prefix = static_cast<int*>(workspace);
     p.seq_order = reinterpret_cast<int*>(static_cast<char*>(workspace) +
@@ -439,6 +443,37 @@ pkv_status pkv_paged_multi_query_attention(
     const int64_t items = mq_max_items(num_seqs, total_q, group, num_kv_heads);
     return cuda_status(launch_mq_attention(p, q_dtype, items, dev->num_sms,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+pkv_status pkv_paged_multi_query_attention(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* query_start, int num_seqs, int total_q,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+    int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
+    pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
+    pkv_stream_t stream) {
+    return multi_query_attention(query, k_cache, v_cache, block_tables, context_lens,
+                                 query_start, nullptr, num_seqs, total_q, num_q_heads,
+                                 num_kv_heads, head_dim, block_size, num_blocks,
+                                 max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype,
+                                 kv_scale, workspace, workspace_bytes, out, stream);
+}
+
+pkv_status pkv_paged_tree_attention(
+    const void* query, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* query_start, const uint64_t* tree_mask,
+    int num_seqs, int total_q, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int num_blocks, int max_blocks_per_seq, int max_context_len, float scale, pkv_dtype q_dtype,
+    pkv_dtype kv_dtype, float kv_scale, void* workspace, size_t workspace_bytes, void* out,
+    pkv_stream_t stream) {
+    if (!tree_mask && num_seqs > 0 && total_q > 0) return PKV_ERR_INVALID_ARG;
+    return multi_query_attention(query, k_cache, v_cache, block_tables, context_lens,
+                                 query_start, tree_mask, num_seqs, total_q, num_q_heads,
+                                 num_kv_heads, head_dim, block_size, num_blocks,
+                                 max_blocks_per_seq, max_context_len, scale, q_dtype, kv_dtype,
+                                 kv_scale, workspace, workspace_bytes, out, stream);
 }
 
 }  // extern "C"

@@ -71,6 +71,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 256;
 constexpr float kMaxSlack = 8.0f;                     // log2-domain headroom before the max moves
+constexpr int kMaxTree = 64;                          // draft tokens of a tree (one uint64 of bits)
 
 static_assert(kMqRows == 2 * kTile, "a CTA holds two row tiles");
 static_assert(kRowRegs * 256 + kAuxRegs * 128 <= (65536 / kThreads) / 8 * 8 * kThreads,
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(1024) mq_plan_kernel(MqParams p) {
             const int n = p.query_start[s + 1] - p.query_start[s];
             const int ctx = p.context_lens[s];
             if (n < 0 || ctx < n || ctx > cap || p.query_start[s] < 0 ||
-                p.query_start[s + 1] > total_q) {
+                p.query_start[s + 1] > total_q || (p.tree && n > kMaxTree)) {
                 set_status(p.status, PKV_DEV_BAD_CONTEXT);
             } else {
                 items = (n * p.group + kMqRows - 1) / kMqRows * p.num_kv_heads;
@@ -473,7 +474,8 @@ __device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_
     }
 }
 
-template <typename QT>
+// TREE: draft-tree verification (the ancestor masks of p.tree) instead of causal attention.
+template <typename QT, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     MqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const __grid_constant__ CUtensorMap tmQ) {
@@ -564,6 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             const int64_t qrow = ((int64_t)(it.q_begin + qi) * p.num_q_heads + it.kvh * G + r % G) * kHD;
             // the last token the row sees (rows past the last query see no further)
             const int lim_row = min(it.ctx - it.n + qi, (X ? it.kv_end_b : it.kv_end_a) - 1);
+            // draft trees: the row sees tree token u < qi (position c0 + u; u < 64) only
+            // when bit u of its ancestor mask is set; tiles reaching the tree need the mask
+            constexpr bool has_tree = TREE;
+            const int c0 = it.ctx - it.n;
+            const uint64_t tree_w = has_tree && row_valid ? __ldg(&p.tree[it.q_begin + qi]) : 0ull;
             // the V rows past the item's last token hold poison or stale data (0 x NaN
             // would reach O through P = 0): the row tile whose P.V reads the last V tile
             // first zeroes them once their copy has landed
@@ -578,15 +585,21 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 // local tokens <= lim are visible; a tile every row of the warp sees whole
                 // needs no mask
                 const int lim = lim_row - j * kTile;
-                const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1);
+                const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1) ||
+                                    (has_tree && (j + 1) * kTile > c0);
                 uint32_t sv[4][32];
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) tc5::ld_32x32b_x32(colS + (uint32_t)(32 * c4), sv[c4]);
                 tc5::wait_ld();
                 if (masked) {
+                    const int u0 = j * kTile - c0;        // tree index of column 0
 #pragma unroll
-                    for (int c = 0; c < kTile; ++c)
-                        if (c > lim) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                    for (int c = 0; c < kTile; ++c) {
+                        const int u = u0 + c;
+                        const bool hidden =
+                            c > lim || (has_tree && u >= 0 && u < qi && !((tree_w >> u) & 1ull));
+                        if (hidden) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                    }
                 }
                 // row max of the raw scores (the scale is positive: same order): four
                 // independent partial maxima, two scores per three-input max
@@ -718,9 +731,13 @@ cudaError_t launch_typed(const MqParams& p, int64_t max_items, int num_ctas, cud
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kernel = mq_attention_kernel<QT>;
+    auto kernel = p.tree ? mq_attention_kernel<QT, true> : mq_attention_kernel<QT, false>;
     if (!attr_set[dev]) {
-        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        err = cudaFuncSetAttribute(mq_attention_kernel<QT, false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(mq_attention_kernel<QT, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
         attr_set[dev] = true;
     }

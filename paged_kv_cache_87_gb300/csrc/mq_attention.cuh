@@ -16,6 +16,7 @@ struct MqParams {
     const int32_t* block_tables;   // [S, max_blocks]
     const int32_t* context_lens;   // [S]: tokens in the cache, the queries' own included
     const int32_t* query_start;    // [S + 1]: query rows of sequence s
+    const uint64_t* tree;          // [total_q] draft-tree ancestor bits, or null (causal)
     void* out;                     // [total_q, Hq, d]
     int* item_prefix;              // workspace [S + 1]: items before the k-th launched sequence
     int* seq_order;                // workspace [S]: the sequence launched k-th

@@ -129,6 +129,8 @@ class MultiQueryState:
         self.block_tables = torch.from_numpy(w.block_tables).to(dev)
         self.context_lens = torch.from_numpy(w.context_lens).to(dev)
         self.query_start = torch.from_numpy(w.query_start).to(dev)
+        self.tree = (torch.from_numpy(w.tree.view(np.int64)).to(dev)
+                     if getattr(w, "tree", None) is not None else None)
         self.new_key = host_tensor(w.key[w.new_idx], w.kv_dtype).to(dev)
         self.new_value = host_tensor(w.value[w.new_idx], w.kv_dtype).to(dev)
         self.new_slots = torch.from_numpy(np.ascontiguousarray(w.slots[w.new_idx])).to(dev)
@@ -153,6 +155,11 @@ class MultiQueryState:
 
     def attend(self, stream=None, out=None) -> torch.Tensor:
         w = self.w
+        if self.tree is not None:
+            return binding.pkv_paged_tree_attention(
+                self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+                self.query_start, self.tree, w.max_context_len, w.scale,
+                workspace=self.workspace, out=self.out if out is None else out, stream=stream)
         return binding.pkv_paged_multi_query_attention(
             self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
             self.query_start, w.max_context_len, w.scale, workspace=self.workspace,

@@ -120,6 +120,29 @@ def test_multi_query_host_validation(lib):
     assert binding.pkv_multi_query_workspace_bytes(1000) == 8448
 
 
+def _tree(lib, tree, **kw):
+    a = dict(query=1024, k=1024, v=1024, bt=1024, cl=1024, qs=1024, S=4, tq=16, Hq=8, Hkv=2,
+             d=128, B=16, NB=64, mb=16, mctx=256, scale=0.088, qt=2, kt=2, kvs=1.0, ws=4096,
+             wsb=4096, out=1024)
+    a.update(kw)
+    return lib.pkv_paged_tree_attention(
+        a["query"], a["k"], a["v"], a["bt"], a["cl"], a["qs"], tree, a["S"], a["tq"], a["Hq"],
+        a["Hkv"], a["d"], a["B"], a["NB"], a["mb"], a["mctx"], a["scale"], a["qt"], a["kt"],
+        a["kvs"], a["ws"], a["wsb"], a["out"], None)
+
+
+def test_tree_host_validation(lib):
+    """The draft-tree entry validates like the causal one and needs an 8-byte aligned mask
+    (checked before any device call)."""
+    E = binding
+    assert _tree(lib, None) == E.PKV_ERR_INVALID_ARG                 # no mask
+    assert _tree(lib, 1028) == E.PKV_ERR_INVALID_ARG                 # misaligned mask
+    assert _tree(lib, 1024, qt=0, kt=0) == E.PKV_ERR_UNSUPPORTED      # fp32
+    assert _tree(lib, 1024, Hq=6) == E.PKV_ERR_UNSUPPORTED
+    assert _tree(lib, 1024, ws=None, wsb=0) == E.PKV_ERR_WORKSPACE
+    assert _tree(lib, None, tq=0, query=None) == E.PKV_OK            # nothing to do
+
+
 def test_reshape_and_copy_host_validation(lib):
     E = binding
     f = lib.pkv_reshape_and_cache

@@ -225,3 +225,96 @@ def test_launch_order_leaves_every_sequence_bit_identical():
     b = _gpu(w2).out
     assert binding.pkv_get_device_status() == 0
     assert torch.equal(a[torch.from_numpy(rows).to(a.device)], b)
+
+
+# ------------------------------------------------------------ draft trees --
+
+def _oracle_tree(w, sel=None):
+    kc, vc = _oracle_pool(w)
+    return oracle.paged_tree_attention(
+        w.query, kc, vc, w.block_tables, w.context_lens, w.query_start, w.tree,
+        num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+        block_size=w.block_size, num_blocks=w.num_blocks, scale=w.scale, q_dtype=w.q_dtype,
+        kv_dtype=w.kv_dtype, sel=sel, nthreads=8)
+
+
+def _check_tree(w):
+    st = _gpu(w)
+    got = st.out_f64()
+    ref = _oracle_tree(w)
+    assert binding.pkv_get_device_status() == 0
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= TOL[w.q_dtype], err
+    return st
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 2), (32, 8), (16, 1)])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_draft_trees_groups_dtypes_block_sizes(dt, Hq, Hkv, B):
+    rng = np.random.default_rng(Hq * 100 + Hkv * 10 + B)
+    w = inputs.make_tree_verify("trees", rng, [0, 130, 700, 64], [17, 64, 33, 1],
+                                kinds=["random", "random", "star", "chain"], num_q_heads=Hq,
+                                num_kv_heads=Hkv, head_dim=128, block_size=B, dtype=dt)
+    _check_tree(w)
+
+
+def test_draft_trees_straddling_kv_tiles():
+    """Trees whose tokens cross a 128-token K/V tile boundary (prior context 100, 200)."""
+    rng = np.random.default_rng(41)
+    w = inputs.make_tree_verify("straddle", rng, [100, 200, 1000], [64, 50, 40],
+                                num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                                dtype="bf16")
+    _check_tree(w)
+
+
+def test_chain_tree_equals_the_causal_kernel_bit_for_bit():
+    rng = np.random.default_rng(42)
+    w = inputs.make_tree_verify("chain", rng, [300, 5, 2000], [40, 9, 64],
+                                kinds=["chain"] * 3, num_q_heads=16, num_kv_heads=4,
+                                head_dim=128, block_size=16, dtype="bf16")
+    a = _gpu(w).out.clone()
+    b = _gpu(inputs.MultiQueryWorkload(**{**w.__dict__, "tree": None})).out
+    assert torch.equal(a, b)
+
+
+def test_tree_of_more_than_64_tokens_is_flagged_and_skipped():
+    rng = np.random.default_rng(43)
+    w = inputs.make_multi_query("big tree", rng, [50, 80], [65, 20], num_q_heads=4,
+                                num_kv_heads=2, head_dim=128, block_size=16, dtype="bf16")
+    w.tree = np.concatenate([np.zeros(65, np.uint64),
+                             inputs.tree_ancestors(inputs.random_tree_parents(rng, 20))])
+    st = MultiQueryState(w)
+    st.run_setup()
+    st.append_step()
+    st.out.fill_(7.0)
+    binding.pkv_get_device_status()
+    st.attend()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_CONTEXT
+    assert torch.all(st.out[:65] == 7.0)
+    ref = oracle.paged_tree_attention(
+        w.query[65:], *_oracle_pool(w), w.block_tables[1:], w.context_lens[1:],
+        w.query_start[1:] - 65, w.tree[65:], num_q_heads=4, num_kv_heads=2, head_dim=128,
+        block_size=16, num_blocks=w.num_blocks, scale=w.scale, q_dtype="bf16", kv_dtype="bf16")
+    assert np.abs(st.out_f64()[65:] - ref).max() <= TOL["bf16"]
+
+
+def test_tree_verification_workload_sampled():
+    """The benchmark's draft-tree workload at full size: sampled rows of every sequence."""
+    w = inputs.make_multi_query_config(3)
+    st = _gpu(w)
+    assert binding.pkv_get_device_status() == 0
+    got = st.out_f64()
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(1)
+    rows = []
+    for s in range(w.num_seqs):
+        q0, q1 = int(w.query_start[s]), int(w.query_start[s + 1])
+        rows += [q0, q1 - 1] + list(rng.integers(q0, q1, size=2))
+    sel = np.array([(r, int(h)) for r in rows for h in rng.integers(0, w.num_q_heads, size=2)],
+                   dtype=np.int32)
+    ref = _oracle_tree(w, sel=sel)
+    err = np.abs(got[sel[:, 0], sel[:, 1]] - ref).max()
+    assert err <= TOL["bf16"], err
