@@ -442,7 +442,7 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-MQ_METRIC = "multi-query causal paged attention: TFLOP/s (of measured bf16 dense peak)"
+MQ_METRIC = "multi-query paged attention (causal or draft tree): TFLOP/s"
 
 
 def measured_tensor_peak():
