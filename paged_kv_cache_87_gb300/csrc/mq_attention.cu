@@ -37,6 +37,10 @@
 // overwrite P_X without a further wait.
 // The running max only moves when a tile's max exceeds it by more than 2^8 (in
 // the log2 domain), and O is rescaled in TMEM only then.
+// Draft-tree verification (§9 speculative decoding trees: each draft token sees
+// the prior context, itself and its ancestors) is a second instantiation: every
+// row holds its uint64 of ancestor bits and the tiles reaching the tree take the
+// masked path.
 // Every mbarrier wait is bounded (2 s); on a timeout the CTA flags
 // PKV_DEV_WAIT_TIMEOUT, drains its MMAs and releases its TMEM.
 #include <type_traits>

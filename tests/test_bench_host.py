@@ -84,3 +84,15 @@ def test_peak_falls_back_without_measured_file(tmp_path, monkeypatch):
     assert bench.measured_peak() == (bench.FALLBACK_HBM_GBS, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6785.2}))
     assert bench.measured_peak()[0] == 6785.2
+
+
+def test_multi_query_roofline_bound_follows_arithmetic_intensity():
+    """The chunked prefill (about 1,350 FLOP per algorithmic byte) is tensor-bound, the
+    draft-tree workload (about 240) HBM-bound, against the ridge of the measured peaks."""
+    from paged_kv_cache_87_gb300 import inputs
+    r1 = bench.mq_roofline(inputs.make_multi_query_config(1), 500e-6)
+    r3 = bench.mq_roofline(inputs.make_multi_query_config(3), 300e-6)
+    assert r1["bound"] == "tensor" and r1["unit"] == "TFLOP/s"
+    assert r3["bound"] == "hbm" and r3["unit"] == "GB/s"
+    assert r3["flops_per_byte"] < r3["ridge_flops_per_byte"] < r1["flops_per_byte"]
+    assert r3["achieved"] == pytest.approx(r3["algorithmic_bytes"] / 300e-6 / 1e9, rel=1e-3)
