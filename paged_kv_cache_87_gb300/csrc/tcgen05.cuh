@@ -34,28 +34,16 @@ __device__ __forceinline__ void fence_after_sync() {
 // ----------------------------------------------------------- descriptors --
 
 // Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B,
-// 1024-byte aligned): start address, leading- and stride-dimension byte
-// offsets (16-byte units), descriptor version 1, layout type 2 (128B swizzle).
-//  * K-major operand (rows of the M/N dimension, 128 B of K per atom row): the
-//    leading offset is unused; `sbo` = bytes between 8-row groups (1024).
-//  * MN-major operand (rows of the K dimension, 64 16-bit MN elements per atom
-//    row): `lbo` = bytes between 64-element MN chunks, `sbo` = bytes between
-//    8-row K groups.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// The same descriptor as two 32-bit words, so that a run of MMAs stepping
+// 1024-byte aligned), as two 32-bit words, so that a run of MMAs stepping
 // through an operand only adds a constant to the low word (start address >> 4
 // in bits 0-13: no carry while the address stays below 256 KB):
-//   low  = start address >> 4 | (LBO >> 4) << 16,
-//   high = SBO >> 4 | version 1 << 14 | layout type 2 << 29.
+//   low  = start address >> 4 | (LBO >> 4) << 16  (leading-dimension byte offset),
+//   high = SBO >> 4 | version 1 << 14 | layout type 2 (128B swizzle) << 29.
+//  * K-major operand (rows of the M/N dimension, 128 B of K per atom row): the
+//    leading offset is unused; SBO = bytes between 8-row groups.
+//  * MN-major operand (rows of the K dimension, 64 16-bit MN elements per atom
+//    row): LBO = bytes between 64-element MN chunks, SBO = bytes between 8-row
+//    K groups.
 __device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t saddr, uint32_t lbo) {
     return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -74,31 +62,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool a
 
 // ------------------------------------------------------------------- MMA --
 
-// D[tmem] (+)= A[smem] . B[smem]^T for one M x N x 16 step; issued by one thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] . B[smem]^T for one M x N x 16 step: A's M rows are TMEM
-// lanes, its 16 K elements (16-bit) packed two per 32-bit column, 8 columns from
-// `a_tmem`; issued by one thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-        : "memory");
-}
-
-// mma_ss / mma_ts with the B (and A) descriptors given as (low, high) words.
+// One M x N x 16 step D[tmem] (+)= A . B^T, issued by one thread: mma_ss_w with A
+// and B in shared memory, mma_ts_w with A in TMEM (its M rows are TMEM lanes, its 16
+// K elements packed two per 32-bit column, 8 columns from `a_tmem`); descriptors
+// as (low, high) words.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                          uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                          uint32_t accumulate) {
