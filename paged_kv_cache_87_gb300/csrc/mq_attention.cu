@@ -591,9 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 const int lim = lim_row - j * kTile;
                 const bool masked = !__all_sync(0xffffffffu, lim >= kTile - 1) ||
                                     (has_tree && (j + 1) * kTile > c0);
-                uint32_t sv[4][32];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tc5::ld_32x32b_x32(colS + (uint32_t)(32 * c4), sv[c4]);
+                uint32_t sv[2][64];
+                tc5::ld_32x32b_x64(colS, sv[0]);
+                tc5::ld_32x32b_x64(colS + 64u, sv[1]);
                 tc5::wait_ld();
                 if (masked) {
                     const int u0 = j * kTile - c0;        // tree index of column 0
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                         const int u = u0 + c;
                         const bool hidden =
                             c > lim || (has_tree && u >= 0 && u < qi && !((tree_w >> u) & 1ull));
-                        if (hidden) sv[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+                        if (hidden) sv[c >> 6][c & 63] = __float_as_uint(-INFINITY);
                     }
                 }
                 // row max of the raw scores (the scale is positive: same order): four
@@ -612,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 for (int i = 0; i < 4; ++i) pmx[i] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < kTile; c += 2)
-                    pmx[(c >> 1) & 3] = max3(pmx[(c >> 1) & 3], __uint_as_float(sv[c >> 5][c & 31]),
-                                             __uint_as_float(sv[c >> 5][(c + 1) & 31]));
+                    pmx[(c >> 1) & 3] = max3(pmx[(c >> 1) & 3], __uint_as_float(sv[c >> 6][c & 63]),
+                                             __uint_as_float(sv[c >> 6][(c + 1) & 63]));
                 const float mx = max3(pmx[0], pmx[1], fmaxf(pmx[2], pmx[3])) * p.qk_scale_log2;
                 const float m_new = mx > m_run + kMaxSlack ? mx : m_run;
                 const bool resc = j > 0 && m_new != m_run;
@@ -641,21 +641,21 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 uint64_t pls[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) pls[i] = 0ull;
+                uint32_t pw[64];                          // the row's 128 weights, packed
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pw[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int c = 64 * hh + 2 * e;
-                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[c >> 5][c & 31]),
-                                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])),
+                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[c >> 6][c & 63]),
+                                                          __uint_as_float(sv[c >> 6][(c + 1) & 63])),
                                                   scale2, negm2);
                         const float a = fast_exp2(f2_lo(x)), bb = fast_exp2(f2_hi(x));
-                        pw[e] = pack2_bits<QT>(a, bb);
+                        pw[32 * hh + e] = pack2_bits<QT>(a, bb);
                         pls[e & 3] = f2_add(pls[e & 3], f2_pack(a, bb));
                     }
-                    tc5::st_32x32b_x32(colS + (uint32_t)(32 * hh), pw);
                 }
+                tc5::st_32x32b_x64(colS, pw);
                 const uint64_t l2 = f2_add(f2_add(pls[0], pls[1]), f2_add(pls[2], pls[3]));
                 l_run += f2_lo(l2) + f2_hi(l2);
                 if (zeroes && j == it.T - 1 && it.kv_end - j * kTile < kTile) {
