@@ -334,6 +334,16 @@ PKV_API pkv_status pkv_paged_decode_attention_noalloc(
     pkv_dtype q_dtype, pkv_dtype kv_dtype, float kv_scale, void* out, pkv_stream_t stream);
 
 /*
+ * Self-test of the pipeline waits: launches one CTA on `stream` whose mbarrier
+ * wait can never complete (nothing arrives at it).  The wait gives up after the
+ * bound every kernel's waits use (2 s of device time), the kernel sets
+ * PKV_DEV_WAIT_TIMEOUT in the device status word (read it with
+ * pkv_get_device_status) and returns: a stalled pipeline reports an error
+ * instead of hanging, and the context stays usable.
+ */
+PKV_API pkv_status pkv_selftest_wait_bound(pkv_stream_t stream);
+
+/*
  * Read and clear the status word of the current device (a bit-or of
  * PKV_DEV_* flags set by kernels since the last read).  Synchronous: waits
  * for the device's work to finish.  `host_code` is a host pointer.

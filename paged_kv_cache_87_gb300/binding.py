@@ -70,6 +70,7 @@ _SIGNATURES = {
         ctypes.c_int,
         [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_int, ctypes.c_void_p]),
     "pkv_get_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint)]),
+    "pkv_selftest_wait_bound": (ctypes.c_int, [ctypes.c_void_p]),
     "pkv_swap_blocks": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -421,6 +422,12 @@ def pkv_get_device_status() -> int:
     v = ctypes.c_uint(0)
     _check("pkv_get_device_status", load().pkv_get_device_status(ctypes.byref(v)))
     return int(v.value)
+
+
+def pkv_selftest_wait_bound(stream=None) -> None:
+    """Launch the wait self-test: a kernel whose pipeline wait never completes gives up
+    after the waits' bound (2 s) and sets DEV_WAIT_TIMEOUT in the device status word."""
+    _check("pkv_selftest_wait_bound", load().pkv_selftest_wait_bound(_stream_ptr(stream)))
 
 
 def pkv_status_string(status: int) -> str:

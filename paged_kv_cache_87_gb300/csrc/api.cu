@@ -343,6 +343,12 @@ pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int src_num_blo
     return cuda_status(launch_copy_blocks(p, num_pairs, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_selftest_wait_bound(pkv_stream_t stream) {
+    DeviceInfo* dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    return cuda_status(launch_wait_bound_probe(dev->status, static_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_get_device_status(unsigned int* host_code) {
     if (!host_code) return PKV_ERR_INVALID_ARG;
     DeviceInfo* dev = nullptr;

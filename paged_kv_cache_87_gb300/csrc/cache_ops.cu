@@ -155,4 +155,20 @@ cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t 
     return cudaGetLastError();
 }
 
+// One thread waits on an mbarrier that nothing arrives at: the bounded wait every
+// pipeline uses gives up after kWaitNs and the kernel flags PKV_DEV_WAIT_TIMEOUT.
+__global__ void wait_bound_probe_kernel(unsigned* status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0)) set_status(status, PKV_DEV_WAIT_TIMEOUT);
+    }
+}
+
+cudaError_t launch_wait_bound_probe(unsigned* status, cudaStream_t stream) {
+    wait_bound_probe_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -31,4 +31,8 @@ cudaError_t launch_reshape_and_cache(const ReshapeParams& p, pkv_dtype src, bool
                                      int num_sms, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t stream);
 
+// A kernel whose pipeline wait can never complete: it flags PKV_DEV_WAIT_TIMEOUT in
+// `status` once the wait's bound has passed, and returns.
+cudaError_t launch_wait_bound_probe(unsigned* status, cudaStream_t stream);
+
 }  // namespace pkv
