@@ -27,7 +27,9 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ("pkv_paged_decode_attention", "pkv_reshape_and_cache", "pkv_copy_blocks",
-                 "pkv_decode_workspace_bytes", "pkv_get_device_status", "pkv_status_string"):
+                 "pkv_decode_workspace_bytes", "pkv_get_device_status", "pkv_status_string",
+                 "pkv_paged_multi_query_attention", "pkv_paged_tree_attention",
+                 "pkv_selftest_wait_bound"):
         assert must in names
 
 
@@ -163,6 +165,19 @@ def test_binding_validates_copy_pairs_on_host():
     for bad in ([[1, 2], [3, 2]], [[1, 2], [2, 5]], [[0, 8]], [[-1, 2]]):
         with pytest.raises(ValueError):
             binding.validate_pairs(bad, 8)
+
+
+def test_binding_checks_the_tree_mask_before_any_call():
+    """The tree mask must be 64-bit, one entry per query row; checked before the library
+    is called (no device needed)."""
+    import torch
+    q = torch.zeros(5, 2, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16)
+    i32 = lambda *s: torch.zeros(*s, dtype=torch.int32)
+    for bad in (torch.zeros(5, dtype=torch.int32), torch.zeros(4, dtype=torch.int64),
+                torch.zeros(5, 1, dtype=torch.int64)):
+        with pytest.raises(ValueError):
+            binding.pkv_paged_tree_attention(q, kc, kc, i32(1, 4), i32(1), i32(2), bad, 64, 0.1)
 
 
 def test_product_path_does_not_import_the_oracle():
