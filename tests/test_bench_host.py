@@ -96,3 +96,21 @@ def test_multi_query_roofline_bound_follows_arithmetic_intensity():
     assert r3["bound"] == "hbm" and r3["unit"] == "GB/s"
     assert r3["flops_per_byte"] < r3["ridge_flops_per_byte"] < r1["flops_per_byte"]
     assert r3["achieved"] == pytest.approx(r3["algorithmic_bytes"] / 300e-6 / 1e9, rel=1e-3)
+
+
+def test_oracle_sample_of_a_tree_workload_counts_visible_pairs():
+    """The reference arm's oracle sample on draft trees calls the tree oracle and counts,
+    per sampled row, the prior context, the token itself and its ancestors."""
+    import numpy as np
+    from paged_kv_cache_87_gb300 import inputs
+    w = inputs.make_tree_verify("host trees", np.random.default_rng(3), [20, 7], [9, 5],
+                                kinds=["random", "star"], num_q_heads=4, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="bf16")
+    tflops, secs, flops, desc = bench.mq_oracle_sample(w, 0.05, 2)
+    assert tflops > 0 and secs > 0 and "pairs" in desc
+    per_row = 4 * w.head_dim * np.array(
+        [w.context_lens[s] - (w.query_start[s + 1] - w.query_start[s]) + 1
+         + bin(int(w.tree[r])).count("1")
+         for s in range(w.num_seqs) for r in range(w.query_start[s], w.query_start[s + 1])])
+    assert flops % (4 * w.head_dim) == 0
+    assert per_row.min() * 8 <= flops <= per_row.max() * 10 ** 6
