@@ -9,8 +9,11 @@ ctx * kv_heads * head_dim * element bytes * 2) divided by the step time.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
                   [--impl ours|reference] [--no-cpu-baseline]
 
-Default workload: the OPT-13B-shaped layer decode (64 sequences, 40 heads,
-head_dim 128, fp16, block size 16, context lengths U[512, 2048]).
+Default workload: the long-context split-KV decode (8 sequences, 64 query / 8 kv
+heads, head_dim 128, bf16, block size 32, context lengths U[32768, 131072]), the
+largest of the five; the same JSON line carries a `per_config` object with every
+workload timed the same way (step and decode µs, algorithmic bytes, roofline
+fraction against the measured copy bandwidth).
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path has no exchange step); the value is the bytes of all ranks divided
 by the slowest rank's time.
@@ -45,7 +48,11 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=1)
+    ap.add_argument("--workload", type=int, default=3,
+                    help="0 tiny MHA fp32, 1 OPT-13B-shaped fp16, 2 GQA bf16, 3 long-context "
+                         "split-KV bf16 (default, the largest), 4 FP8 KV + shared prefix")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload (skip the per_config timings of the others)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="shrink the workload to its first N sequences (profiling captures)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -309,10 +316,81 @@ def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int =
 
 # ------------------------------------------------------------------- arms --
 
+def time_decode_steps(torch, st, stream, steps, warmup, flush_buf, world=1, device=None):
+    """Warm up, then time `steps` hot-path steps with CUDA events on `stream`.
+
+    Returns (step ms, decode ms) per timed step; the decode events bracket the
+    decode call alone (planning + decode (+ merge) kernels).  `flush_buf`, when
+    given, is written before every timed step (outside the events) so the step
+    starts with a cold L2."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            st.step(stream)
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(device)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps):
+            if flush_buf is not None:
+                flush_buf.zero_()
+            s0, d0, d1, s1 = ev[i]
+            s0.record(stream)
+            st.copy_step(stream)
+            st.append_step(stream)
+            d0.record(stream)
+            st.decode(stream)
+            d1.record(stream)
+            s1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(world)
+    return [e[0].elapsed_time(e[3]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev]
+
+
+def launches_per_step(w, prefix: bool) -> int:
+    """Kernels one hot-path step launches: copy_blocks (if the step has pairs),
+    reshape_and_cache, the planning and decode kernels, and the merge kernel of a
+    prefix-aware launch on the tensor-core path (16-bit q with K/V of the same
+    type, or e4m3 K/V at head_dim 128)."""
+    mma = w.q_dtype in ("f16", "bf16") and (w.kv_dtype == w.q_dtype or
+                                             (w.kv_dtype == "e4m3" and w.head_dim == 128))
+    return (1 if len(w.step_pairs) else 0) + 1 + 2 + (1 if mma and prefix else 0)
+
+
+def l2_policy(torch, w, device):
+    """Flush buffer (2x L2, written before every timed step) when the workload's KV is
+    smaller than 4x L2; otherwise None (the inputs are larger than L2)."""
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    if w.kv_read_bytes < 4 * l2:
+        return (torch.empty(2 * l2 // 4 * 4, dtype=torch.uint8, device=device),
+                "L2 flushed between steps (write of 2x L2)")
+    return None, f"inputs larger than L2 ({w.kv_read_bytes / 1e9:.2f} GB of KV per step)"
+
+
+def per_config_entry(w, step_ms, dec_ms, peak, l2_note, prefix) -> dict:
+    """One workload's timing: step and decode µs, algorithmic bytes, roofline fraction.
+
+    The roofline's bytes are the unique K/V rows the decode must read (for the
+    shared-prefix workload each shared block once per group); the logical bytes
+    (every sequence's context) give the KV-read rate, which is not a roofline
+    fraction when blocks are shared."""
+    dec_s = float(np.mean(dec_ms)) * 1e-3
+    step_s = float(np.mean(step_ms)) * 1e-3
+    e = {"workload": w.name, "step_us": round(step_s * 1e6, 2), "decode_us": round(dec_s * 1e6, 2),
+         "kv_read_bytes": w.kv_read_bytes, "unique_kv_bytes": w.unique_kv_bytes,
+         "step_kv_read_gbs": round(w.kv_read_bytes / step_s / 1e9, 1),
+         "decode_gbs": round(w.unique_kv_bytes / dec_s / 1e9, 1),
+         "frac": round(w.unique_kv_bytes / dec_s / 1e9 / peak, 4),
+         "l2": l2_note, "entry": "prefix-aware" if prefix else "plain"}
+    if w.unique_kv_bytes != w.kv_read_bytes:
+        e["logical_kv_gbs_not_a_roofline"] = round(w.kv_read_bytes / dec_s / 1e9, 1)
+    return e
+
+
 def run_ours(args, rank, world, local):
     import torch
     from paged_kv_cache_87_gb300 import binding, build, inputs
-    from paged_kv_cache_87_gb300.session import DeviceState, host_tensor
+    from paged_kv_cache_87_gb300.session import DeviceState
 
     build.build()
     torch.cuda.set_device(local)
@@ -323,72 +401,32 @@ def run_ours(args, rank, world, local):
     st.run_setup()
     stream = torch.cuda.Stream(device)
     torch.cuda.synchronize(device)
-
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = w.kv_read_bytes < 4 * l2
-    flush_buf = torch.empty(2 * l2 // 4 * 4 if flush else 4, dtype=torch.uint8, device=device)
-    # copy (if any), append, then plan + decode (+ the merge kernel of a grouped launch on
-    # the tensor-core path: 16-bit q with K/V of the same type, or e4m3 K/V at d = 128)
-    mma = w.q_dtype in ("f16", "bf16") and (w.kv_dtype == w.q_dtype or
-                                             (w.kv_dtype == "e4m3" and w.head_dim == 128))
-    launches_per_step = (1 if len(w.step_pairs) else 0) + 1 + 2 + (1 if mma and st.prefix else 0)
-
-    def step_with_decode_events(dec0, dec1):
-        st.copy_step(stream)
-        st.append_step(stream)
-        dec0.record(stream)
-        st.decode(stream)
-        dec1.record(stream)
+    flush_buf, l2_note = l2_policy(torch, w, device)
+    peak, peak_src = measured_peak()
 
     clocks = ClockSampler(local)
     clocks.start()
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            st.step(stream)
-        stream.synchronize()
-        barrier(world)
-        torch.cuda.synchronize(device)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            if flush:
-                flush_buf.zero_()
-            s0, d0, d1, s1 = ev[i]
-            s0.record(stream)
-            step_with_decode_events(d0, d1)
-            s1.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize(device)
-        barrier(world)
+    step_ms, dec_ms = time_decode_steps(torch, st, stream, args.steps, args.warmup, flush_buf,
+                                        world, device)
     clk = clocks.stop()
     assert binding.pkv_get_device_status() == 0, "device status flagged during the benchmark"
-    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
     sec_step = float(np.mean(step_ms)) * 1e-3
     total_bytes, slowest, value = aggregate(w.kv_read_bytes, sec_step, world, device)
 
-    # end to end: pinned host inputs -> device, the step, result -> host, every step
-    pin = lambda t: t.pin_memory()
-    h_q = pin(host_tensor(w.query, w.q_dtype))
-    h_k = pin(host_tensor(w.key[w.new_vec], w.src_dtype))
-    h_v = pin(host_tensor(w.value[w.new_vec], w.src_dtype))
-    h_slots = pin(torch.from_numpy(w.new_slots))
-    h_ctx = pin(torch.from_numpy(w.context_lens))
-    h_tab = pin(torch.from_numpy(w.block_tables))
-    h_pairs = pin(torch.from_numpy(np.ascontiguousarray(w.step_pairs, np.int32)))
-    h_out = pin(torch.empty_like(st.out, device="cpu"))
-    ins = [(h_q, st.query), (h_k, st.new_key), (h_v, st.new_value), (h_slots, st.new_slots),
-           (h_ctx, st.context_lens), (h_tab, st.block_tables), (h_pairs, st.step_pairs)]
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
-    d2h = h_out.numel() * h_out.element_size()
+    # end to end through the public calls: every step, one host-to-device copy of the
+    # step's inputs (query, new K/V, slots, context lengths, tables, copy pairs) packed
+    # in one pinned buffer, the step, and the output copied back to pinned memory
+    h_in, d_in = st.pack_step_inputs()
+    h_out = torch.empty_like(st.out, device="cpu").pin_memory()
+    h2d, d2h = h_in.numel(), h_out.numel() * h_out.element_size()
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
-            if flush:
+            if flush_buf is not None:
                 flush_buf.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for h, d in ins:
-                d.copy_(h, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
             st.step(stream)
             h_out.copy_(st.out, non_blocking=True)
             b.record(stream)
@@ -397,13 +435,35 @@ def run_ours(args, rank, world, local):
                 e2e_ms.append(a.elapsed_time(b))
     _, _, e2e_value = aggregate(w.kv_read_bytes, float(np.mean(e2e_ms)) * 1e-3, world, device)
 
-    peak, peak_src = measured_peak()
+    head = per_config_entry(w, step_ms, dec_ms, peak, l2_note, st.prefix)
     dec_s = float(np.mean(dec_ms)) * 1e-3
-    achieved = w.kv_read_bytes / dec_s / 1e9
+    achieved = w.unique_kv_bytes / dec_s / 1e9
     copy_peak = copy_peak_gbs(torch, device, stream) if rank == 0 else None
     # DRAM bytes of one decode launch from the committed ncu capture (when it was taken
-    # on this source): the shared-prefix workload reads far fewer bytes than it attends
+    # on this source)
     traffic = recorded_traffic(args.workload) if args.num_seqs is None else None
+    nlaunch = launches_per_step(w, st.prefix)
+    del st, d_in, flush_buf
+    torch.cuda.empty_cache()
+
+    # the other workloads, each timed the same way (same steps, warm-up and L2 policy)
+    per_config = {}
+    if not args.no_per_config and args.num_seqs is None:
+        for cid in range(len(inputs.CONFIG_NAMES)):
+            if cid == args.workload:
+                per_config[str(cid)] = head
+                continue
+            wc = inputs.make_config(cid)
+            sc = DeviceState(wc, device)
+            sc.run_setup()
+            fb, note = l2_policy(torch, wc, device)
+            sm, dm = time_decode_steps(torch, sc, stream, args.steps, args.warmup, fb, world,
+                                       device)
+            assert binding.pkv_get_device_status() == 0, f"device status flagged ({wc.name})"
+            per_config[str(cid)] = per_config_entry(wc, sm, dm, peak, note, sc.prefix)
+            del sc, fb
+            torch.cuda.empty_cache()
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(slowest * 1e3, 5),
@@ -417,22 +477,25 @@ def run_ours(args, rank, world, local):
             "mean_context": float(w.context_lens.mean()),
             "kv_read_bytes_per_step": w.kv_read_bytes,
             "unique_kv_bytes_per_step": w.unique_kv_bytes,
-            "l2": ("L2 flushed between steps (write of 2x L2)" if flush else
-                   f"inputs larger than L2 ({w.kv_read_bytes / 1e9:.2f} GB of KV per step)"),
+            "l2": l2_note,
             "step": "copy_blocks (if any) + reshape_and_cache + paged decode",
             "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
                      "dram_gbs": round(traffic / dec_s / 1e9, 1) if traffic else None,
+                     "algorithmic_bytes": w.unique_kv_bytes,
                      "kernel": "planning + decode kernels (CUDA events around the decode call)",
                      "decode_us": round(dec_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 5)},
-        "gpu_launches": launches_per_step * args.steps,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(float(np.mean(e2e_ms)), 5),
+                "copies_per_step": "one host-to-device (packed inputs), one device-to-host"},
+        "gpu_launches": nlaunch * args.steps,
         "clocks": clk,
         "copy_peak_gbs_same_run": round(copy_peak, 1) if copy_peak else None,
     }
+    if per_config:
+        line["per_config"] = per_config
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, secs, nbytes, threads, desc = oracle_baseline(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
@@ -535,7 +598,7 @@ def run_mq(args, rank, world, local):
     """The multi-query workload: per step, write the queries' own K/V and attend."""
     import torch
     from paged_kv_cache_87_gb300 import binding, build, inputs
-    from paged_kv_cache_87_gb300.session import MultiQueryState, host_tensor
+    from paged_kv_cache_87_gb300.session import MultiQueryState
 
     build.build()
     torch.cuda.set_device(local)
@@ -576,28 +639,18 @@ def run_mq(args, rank, world, local):
     total, slowest, _ = aggregate(w.flops, sec_step, world, device)
     value = total / slowest / 1e12
 
-    # end to end: the step's inputs from pinned host memory, the output back, every step
-    pin = lambda t: t.pin_memory()
-    ins = [(pin(host_tensor(w.query, w.q_dtype)), st.query),
-           (pin(host_tensor(w.key[w.new_idx], w.kv_dtype)), st.new_key),
-           (pin(host_tensor(w.value[w.new_idx], w.kv_dtype)), st.new_value),
-           (pin(torch.from_numpy(np.ascontiguousarray(w.slots[w.new_idx]))), st.new_slots),
-           (pin(torch.from_numpy(w.context_lens)), st.context_lens),
-           (pin(torch.from_numpy(w.query_start)), st.query_start),
-           (pin(torch.from_numpy(w.block_tables)), st.block_tables)]
-    if st.tree is not None:                                   # draft trees: their masks too
-        ins.append((pin(torch.from_numpy(w.tree.view(np.int64))), st.tree))
-    h_out = pin(torch.empty_like(st.out, device="cpu"))
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
-    d2h = h_out.numel() * h_out.element_size()
+    # end to end: one host-to-device copy of the step's inputs packed in one pinned
+    # buffer, the step, the output copied back to pinned memory, every step
+    h_in, d_in = st.pack_step_inputs()
+    h_out = torch.empty_like(st.out, device="cpu").pin_memory()
+    h2d, d2h = h_in.numel(), h_out.numel() * h_out.element_size()
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
             flush_buf.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for h, d in ins:
-                d.copy_(h, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
             st.step(stream)
             h_out.copy_(st.out, non_blocking=True)
             b.record(stream)

@@ -305,9 +305,11 @@ PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int src
 /*
  * Paged decode attention without a caller-provided workspace.  No
  * counterpart on the pages: this entry point exists for callers that cannot
- * allocate device memory at decode time (code running while a CUDA graph is
- * being captured, plugins whose host framework owns all device allocations,
- * hosts with a fixed memory budget).
+ * allocate device memory when they decode -- plugins whose host framework
+ * owns every device allocation (its caching allocator must account for all
+ * memory, so a library may not call cudaMalloc behind its back), servers that
+ * run under a fixed device-memory budget set at start-up, and latency-critical
+ * loops where a cudaMalloc (which may synchronise the device) is not allowed.
  *
  * Same arguments, semantics and errors as pkv_paged_decode_attention, minus
  * `workspace` / `workspace_bytes`.  The workspace is a static device array of
@@ -317,8 +319,11 @@ PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int src
  *     PKV_NOALLOC_SCRATCH_BYTES the call returns PKV_ERR_WORKSPACE and
  *     launches nothing.
  *   - Set-up: the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current).  Make that first call
- *     outside any stream capture.
+ *     (cudaGetSymbolAddress, with that device current), and the first call of
+ *     each (q_dtype, kv_dtype, head_dim) combination on a device sets its
+ *     kernel's shared-memory limit and queries its occupancy.  Make those
+ *     first calls (one warm-up call per combination is enough) before any
+ *     stream capture.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents (each call rewrites what must start at zero before
  *     its kernels read it).  Calls whose kernels overlap on the GPU -- on two
@@ -399,8 +404,10 @@ PKV_API pkv_status pkv_bm_sequence(const pkv_block_manager* m, int64_t seq_id,
  * given order), writing slot_mapping[n], the copy-on-write pairs
  * cow_pairs[*num_cow][2] (room for n), and optionally the updated block_tables
  * [n][max_blocks] (-1 padded) and context_lens[n].  Validates first: on error
- * nothing changes (the free-block check assumes every append into a shared
- * block copies, so it may refuse when exactly enough blocks remain). */
+ * nothing changes.  The free-block check counts exactly the blocks the step
+ * takes: one per full last block, and for a shared block of reference count r
+ * written by k of the n sequences, min(k, r - 1) copies (the last writer to
+ * find it shared becomes its sole owner). */
 PKV_API pkv_status pkv_bm_prepare_step(pkv_block_manager* m, const int64_t* seq_ids, int n,
                                        int64_t* slot_mapping, int32_t* cow_pairs,
                                        int* num_cow, int32_t* block_tables, int max_blocks,

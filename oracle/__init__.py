@@ -31,17 +31,37 @@ _lock = threading.Lock()
 _lib = None
 
 
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math"]
+
+
+def _digest() -> str:
+    """SHA-256 of oracle.c, the gcc flags and `gcc --version`: the build is redone
+    whenever any of them changes."""
+    import hashlib
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(("\x1f".join(_CFLAGS)).encode())
+    h.update(subprocess.run(["gcc", "--version"], capture_output=True, text=True).stdout.encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c with gcc (IEEE arithmetic: no fast-math, no FMA contraction)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
+    stamp = _LIB_PATH + ".sha256"
+    want = _digest()
+    if not force and os.path.exists(_LIB_PATH) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == want:
+                return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    subprocess.run(["gcc", *_CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
+    with open(stamp + f".tmp{os.getpid()}", "w") as f:
+        f.write(want + "\n")
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
     return _LIB_PATH
 
 

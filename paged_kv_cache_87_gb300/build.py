@@ -1,12 +1,15 @@
 """Build libpagedkv.so in-tree with nvcc for sm_103a.
 
 Each .cu file compiles to an object in parallel; the objects link into
-``paged_kv_cache_87_gb300/libpagedkv.so``.  Rebuilds only when a source or
-header is newer than the library.
+``paged_kv_cache_87_gb300/libpagedkv.so``.  The build is content-addressed: a
+SHA-256 over every source and header, the compile and link flags and the
+output of ``nvcc --version`` is stored beside the objects, and the library is
+rebuilt whenever that digest changes (a modification time is never trusted).
 """
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -38,19 +41,47 @@ def _inputs() -> list[str]:
         [os.path.join(ROOT, "include", "pagedkv.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+STAMP = os.path.join(BUILD, "libpagedkv.sha256")
+LINK_FLAGS = ["-shared", "-cudart", "static"]
+_nvcc_version: dict[str, str] = {}
+
+
+def nvcc_version(cc: str) -> str:
+    if cc not in _nvcc_version:
+        r = subprocess.run([cc, "--version"], capture_output=True, text=True)
+        _nvcc_version[cc] = r.stdout + r.stderr
+    return _nvcc_version[cc]
+
+
+def digest(extra_flags: list[str] | None = None, cc: str | None = None) -> str:
+    """SHA-256 of what the library is built from: every input file (name and bytes),
+    the architecture, compile and link flags, and the compiler's version string."""
+    h = hashlib.sha256()
+    for f in sorted(_inputs()):
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    for part in (ARCH, NVCC_FLAGS, extra_flags or [], LINK_FLAGS):
+        h.update(("\x1f".join(part) + "\0").encode())
+    h.update(nvcc_version(cc or nvcc()).encode())
+    return h.hexdigest()
+
+
+def up_to_date(extra_flags: list[str] | None = None) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(f) <= t for f in _inputs())
+    with open(STAMP) as f:
+        return f.read().strip() == digest(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if not force and up_to_date(extra):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    want = digest(extra, cc)
 
     def compile_one(src: str) -> tuple[str, str]:
         obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
@@ -67,11 +98,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log:
                 print(log)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
+    cmd = [cc, *ARCH, *LINK_FLAGS, "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP + f".tmp{os.getpid()}", "w") as f:
+        f.write(want + "\n")
+    os.replace(STAMP + f".tmp{os.getpid()}", STAMP)
     return LIB
 
 

@@ -167,8 +167,13 @@ PKV_API pkv_status pkv_bm_prepare_step(pkv_block_manager* m, const int64_t* seq_
                                        int32_t* context_lens) {
     if (!m || n < 0 || (n && (!seq_ids || !slot_mapping || !cow_pairs || !num_cow)))
         return PKV_ERR_INVALID_ARG;
-    // validate first, so a failure leaves the manager unchanged
+    // validate first, so a failure leaves the manager unchanged.  Blocks the step
+    // takes: one per sequence whose last block is full, and, for a shared block
+    // with reference count r that k of the step's sequences write into, min(k, r-1)
+    // copies -- each writer but the last to find it shared copies it and drops the
+    // count by one, so once it reaches 1 the remaining writer owns it
     int64_t new_blocks = 0;
+    std::unordered_map<int32_t, int64_t> writers;   // shared block -> writers this step
     for (int i = 0; i < n; ++i) {
         auto it = m->seqs.find(seq_ids[i]);
         if (it == m->seqs.end()) return PKV_ERR_INVALID_ARG;
@@ -176,9 +181,17 @@ PKV_API pkv_status pkv_bm_prepare_step(pkv_block_manager* m, const int64_t* seq_
             if (seq_ids[k] == seq_ids[i]) return PKV_ERR_INVALID_ARG;
         const Sequence& s = it->second;
         const int64_t j = s.num_tokens / m->block_size;
-        if (j >= (int64_t)s.blocks.size() || m->refcount[(size_t)s.blocks[(size_t)j]] > 1)
+        if (j >= (int64_t)s.blocks.size()) {
             ++new_blocks;
+        } else {
+            const int32_t b = s.blocks[(size_t)j];
+            if (m->refcount[(size_t)b] > 1) ++writers[b];
+        }
         if (block_tables && (int64_t)s.blocks.size() + 1 > max_blocks) return PKV_ERR_INVALID_ARG;
+    }
+    for (const auto& kv : writers) {
+        const int64_t r = m->refcount[(size_t)kv.first];
+        new_blocks += kv.second < r - 1 ? kv.second : r - 1;
     }
     if (new_blocks > (int64_t)m->free_list.size()) return PKV_ERR_OUT_OF_BLOCKS;
     int ncow = 0;

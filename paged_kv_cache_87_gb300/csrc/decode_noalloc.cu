@@ -2,12 +2,14 @@
 //
 // pkv_paged_decode_attention needs a caller-provided device workspace (the
 // work list, arrival counters and split-KV partial states).  Some callers
-// cannot call cudaMalloc when they decode: code that runs while a CUDA graph
-// is being captured, plugins whose host framework owns every device
-// allocation, or hosts with a fixed memory budget that forbids growing it.
-// For them this file keeps the workspace in a fixed, file-scope device array
-// that the module carries on every device that loads the library, and passes
-// its device address to the same kernels.  Nothing here allocates.
+// cannot call cudaMalloc when they decode: plugins whose host framework owns
+// every device allocation (its caching allocator must see all memory),
+// servers held to a device-memory budget fixed at start-up, and latency-
+// critical loops in which a cudaMalloc, which may synchronise the device, is
+// not allowed.  For them this file keeps the workspace in a fixed, file-scope
+// device array that the module carries on every device that loads the
+// library, and passes its device address to the same kernels.  Nothing here
+// allocates.
 #include <mutex>
 
 #include "../../include/pagedkv.h"

@@ -112,6 +112,41 @@ class DeviceState:
     def out_f64(self) -> np.ndarray:
         return self.out.detach().to(torch.float64).cpu().numpy()
 
+    STEP_INPUTS = ("query", "new_key", "new_value", "new_slots", "context_lens",
+                   "block_tables", "step_pairs")
+
+    def pack_step_inputs(self) -> tuple[torch.Tensor, torch.Tensor]:
+        """Move the step's inputs into one device buffer and return it with a pinned host
+        buffer of the same layout holding their values.
+
+        Each input becomes a 256-byte aligned view of the device buffer, so a single
+        host-to-device copy of the host buffer refreshes every input of a step (instead
+        of one small copy per tensor)."""
+        return pack_views(self, self.STEP_INPUTS)
+
+
+def pack_views(obj, names) -> tuple[torch.Tensor, torch.Tensor]:
+    """Replace the tensors obj.<name> by views of one device byte buffer (256-byte
+    aligned offsets, values kept); returns (pinned host copy, device buffer)."""
+    tensors = [getattr(obj, n) for n in names]
+    offs, off = [], 0
+    for t in tensors:
+        off = (off + 255) // 256 * 256
+        offs.append(off)
+        off += t.numel() * t.element_size()
+    dev = torch.empty(max(off, 256), dtype=torch.uint8, device=tensors[0].device)
+    host = torch.empty(dev.numel(), dtype=torch.uint8).pin_memory()
+    host.zero_()
+    for n, t, o in zip(names, tensors, offs):
+        nb = t.numel() * t.element_size()
+        view = dev[o:o + nb].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        if nb:
+            host[o:o + nb].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        setattr(obj, n, view)
+    torch.cuda.synchronize(dev.device)
+    return host, dev
+
 
 class MultiQueryState:
     """A multi-query workload's pool, tables and queries resident on one CUDA device.
@@ -169,6 +204,13 @@ class MultiQueryState:
         """One pass: write the queries' own K/V, then attend."""
         self.append_step(stream)
         return self.attend(stream)
+
+    def pack_step_inputs(self) -> tuple[torch.Tensor, torch.Tensor]:
+        """As DeviceState.pack_step_inputs: the step's inputs as views of one device
+        buffer, plus a pinned host buffer of the same layout."""
+        names = ["query", "new_key", "new_value", "new_slots", "context_lens", "query_start",
+                 "block_tables"] + (["tree"] if self.tree is not None else [])
+        return pack_views(self, names)
 
     def out_f64(self) -> np.ndarray:
         return self.out.detach().to(torch.float64).cpu().numpy()

@@ -115,3 +115,41 @@ def test_oracle_sample_of_a_tree_workload_counts_visible_pairs():
     assert flops % (4 * w.head_dim) == 0
     k = flops // min(per_row)                               # sampled pairs: at least 8
     assert k >= 8 and min(per_row) * 8 <= flops
+
+
+def test_per_config_entry_uses_unique_bytes_for_the_roofline():
+    """The roofline fraction divides the unique K/V rows (each shared prompt block once)
+    by the decode time; the logical rate of a shared-prefix workload is labelled as not
+    a roofline, and is absent when nothing is shared."""
+    from types import SimpleNamespace
+    w = SimpleNamespace(name="shared", kv_read_bytes=4_000_000_000,
+                        unique_kv_bytes=1_000_000_000)
+    e = bench.per_config_entry(w, [0.5, 0.5], [0.25, 0.25], 8000.0, "flushed", True)
+    assert e["decode_us"] == pytest.approx(250.0)
+    assert e["step_us"] == pytest.approx(500.0)
+    assert e["decode_gbs"] == pytest.approx(4000.0)
+    assert e["frac"] == pytest.approx(0.5)
+    assert e["logical_kv_gbs_not_a_roofline"] == pytest.approx(16000.0)
+    assert e["entry"] == "prefix-aware"
+    w2 = SimpleNamespace(name="plain", kv_read_bytes=10**9, unique_kv_bytes=10**9)
+    e2 = bench.per_config_entry(w2, [1.0], [0.5], 4000.0, "flushed", False)
+    assert e2["frac"] == pytest.approx(0.5) and "logical_kv_gbs_not_a_roofline" not in e2
+
+
+def test_launch_count_per_step():
+    from types import SimpleNamespace
+    import numpy as np
+    w = SimpleNamespace(q_dtype="bf16", kv_dtype="e4m3", head_dim=128,
+                        step_pairs=np.zeros((32, 2), np.int32))
+    assert bench.launches_per_step(w, True) == 5       # copy, append, plan, decode, merge
+    assert bench.launches_per_step(w, False) == 4
+    w.step_pairs = np.zeros((0, 2), np.int32)
+    w.q_dtype, w.kv_dtype = "f32", "f32"
+    assert bench.launches_per_step(w, True) == 3       # append, plan, decode (CUDA cores)
+
+
+def test_default_workload_is_the_long_context_split_kv_decode():
+    args = bench.parse_args([])
+    assert args.workload == 3
+    from paged_kv_cache_87_gb300 import inputs
+    assert "long-context split-KV" in inputs.CONFIG_NAMES[args.workload]

@@ -159,3 +159,36 @@ def test_prepare_step_batches_appends_and_cow():
     assert sorted(tables[:3, 2].tolist()) == sorted(pairs[:, 1].tolist())
     assert (tables[:, :2] == [0, 1]).all() and (tables[:, 3:] == -1).all()
     binding.validate_pairs(pairs, 64)
+
+
+def test_prepare_step_needs_only_the_copies_it_makes():
+    """Two sequences share a partial last block (refcount 2) and one block is free: the
+    first writer copies it, the second becomes its sole owner, so the step fits."""
+    B = 16
+    m = binding.BlockManager(3, B)
+    m.add_sequence(0, 20)                  # blocks 0, 1 (the second partial)
+    m.fork(0, 1)
+    assert m.num_free == 1
+    slots, pairs, tables, ctx = m.prepare_step([0, 1], 4)
+    assert len(pairs) == 1 and pairs[0][0] == 1 and pairs[0][1] == 2
+    assert m.num_free == 0 and m.refcount(1) == 1 and m.refcount(2) == 1
+    assert (ctx == 21).all()
+    # three sharers of one block and a single free block: two copies are needed
+    m2 = binding.BlockManager(4, B)
+    m2.add_sequence(0, 20)
+    m2.fork(0, 1)
+    m2.fork(0, 2)
+    assert m2.num_free == 2
+    before = [m2.refcount(b) for b in range(4)]
+    slots, pairs, tables, ctx = m2.prepare_step([0, 1, 2], 4)
+    assert len(pairs) == 2 and m2.num_free == 0
+    m3 = binding.BlockManager(3 + 1, B)
+    m3.add_sequence(0, 20)
+    m3.fork(0, 1)
+    m3.fork(0, 2)
+    m3.add_sequence(9, 1)                  # takes one of the two free blocks
+    assert m3.num_free == 1
+    before = [m3.refcount(b) for b in range(4)]
+    with pytest.raises(binding.PagedKVError):
+        m3.prepare_step([0, 1, 2], 4)      # two copies, one free block: refused
+    assert [m3.refcount(b) for b in range(4)] == before and m3.num_free == 1

@@ -35,8 +35,10 @@ def test_shared_prefix_groups_bf16(samples, Hq, Hkv, B):
     _check(w)
 
 
-@pytest.mark.parametrize("dt,kv,d", [("f16", "f16", 64), ("bf16", "e4m3", 128),
-                                     ("f16", "e4m3", 128)])
+@pytest.mark.parametrize("dt,kv,d", [("f16", "f16", 64), ("f16", "f16", 128),
+                                     ("bf16", "bf16", 64), ("bf16", "e4m3", 128),
+                                     ("f16", "e4m3", 128), ("f32", "f32", 64),
+                                     ("f32", "e4m3", 128), ("bf16", "e4m3", 64)])
 def test_shared_prefix_groups_types(dt, kv, d):
     rng = np.random.default_rng(7)
     w = inputs.make_shared_prefix("prefix", rng, num_groups=4, samples=4, prefix_lo=64,

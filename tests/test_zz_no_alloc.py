@@ -1,9 +1,10 @@
 """pkv_paged_decode_attention_noalloc: decode for callers that cannot allocate.
 
-Callers that run while a CUDA graph is captured, or inside a host framework
-that owns every device allocation, cannot hand the decode a cudaMalloc'ed
-workspace.  This entry point uses the library's static device scratch
-instead.  Its output must match the workspace entry point's on the same
+Callers inside a host framework that owns every device allocation, under a
+device-memory budget fixed at start-up, or in a loop where a cudaMalloc (which
+may synchronise the device) is not allowed cannot hand the decode a
+cudaMalloc'ed workspace.  This entry point uses the library's static device
+scratch instead.  Its output must match the workspace entry point's on the same
 inputs, call after call (the scratch keeps the previous call's contents), and
 it must refuse sizes that need more scratch than the array holds.
 
