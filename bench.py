@@ -349,22 +349,24 @@ def time_decode_steps(torch, st, stream, steps, warmup, flush_buf, world=1, devi
 
 def launches_per_step(w, prefix: bool) -> int:
     """Kernels one hot-path step launches: copy_blocks (if the step has pairs),
-    reshape_and_cache, the planning and decode kernels, and the merge kernel of a
-    prefix-aware launch on the tensor-core path (16-bit q with K/V of the same
-    type, or e4m3 K/V at head_dim 128)."""
+    reshape_and_cache, the planning and decode kernels, and for a prefix-aware launch
+    on the tensor-core path (16-bit q with K/V of the same type, or e4m3 K/V at
+    head_dim 128; at most 8 query heads per kv head) the shared-prefix detection and
+    the merge kernel."""
     mma = w.q_dtype in ("f16", "bf16") and (w.kv_dtype == w.q_dtype or
                                              (w.kv_dtype == "e4m3" and w.head_dim == 128))
-    return (1 if len(w.step_pairs) else 0) + 1 + 2 + (1 if mma and prefix else 0)
+    grouped = mma and prefix and w.num_q_heads // w.num_kv_heads <= 8
+    return (1 if len(w.step_pairs) else 0) + 1 + 2 + (2 if grouped else 0)
 
 
 def l2_policy(torch, w, device):
     """Flush buffer (2x L2, written before every timed step) when the workload's KV is
     smaller than 4x L2; otherwise None (the inputs are larger than L2)."""
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    if w.kv_read_bytes < 4 * l2:
+    if w.unique_kv_bytes < 4 * l2:
         return (torch.empty(2 * l2 // 4 * 4, dtype=torch.uint8, device=device),
                 "L2 flushed between steps (write of 2x L2)")
-    return None, f"inputs larger than L2 ({w.kv_read_bytes / 1e9:.2f} GB of KV per step)"
+    return None, f"inputs larger than L2 ({w.unique_kv_bytes / 1e9:.2f} GB of distinct KV per step)"
 
 
 def per_config_entry(w, step_ms, dec_ms, peak, l2_note, prefix) -> dict:

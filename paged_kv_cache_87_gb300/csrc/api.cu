@@ -61,8 +61,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct Plan {
     int group, hpi, nsub;
     int chunk_tokens, max_chunks, part_stride;
-    size_t off_hdr, off_ctx, off_items, off_recp, off_recc, off_workers, off_seq, off_units,
-        off_expect, off_pm, off_pl, off_pacc, total;
+    size_t off_hdr, off_ctx, off_items, off_recp, off_recc, off_workers, off_seq, off_common,
+        off_units, off_expect, off_pm, off_pl, off_pacc, total;
 };
 
 // Chunk length: at least 512 tokens, a multiple of 64 (every stage size and
@@ -97,6 +97,7 @@ pkv_status make_plan(int S, int Hq, int Hkv, int HD, int B, int max_ctx, Plan* p
     p.off_recc = off;    off = round_up(off + 2 * s * 16, 256);
     p.off_workers = off; off = round_up(off + (size_t)kMaxWorkers * 32, 256);
     p.off_seq = off;     off = round_up(off + s * 16, 256);
+    p.off_common = off;  off = round_up(off + s * 4, 256);
     p.off_units = off;   off = round_up(off + units * 4, 256);
     p.off_expect = off;  off = round_up(off + units * 4, 256);
     const size_t partial_states = max_ctx > 0 ? s * Hq * (size_t)p.part_stride : 0;
@@ -181,6 +182,7 @@ pkv_status decode_impl(const void* query, const void* k_cache, const void* v_cac
     p.ws.rec = reinterpret_cast<int4*>(ws + plan.off_recc);
     p.ws.worker_first = reinterpret_cast<int4*>(ws + plan.off_workers);
     p.ws.seq_info = reinterpret_cast<int4*>(ws + plan.off_seq);
+    p.ws.common = reinterpret_cast<int*>(ws + plan.off_common);
     p.ws.unit_expect = reinterpret_cast<int*>(ws + plan.off_expect);
     p.ws.unit_done = reinterpret_cast<unsigned*>(ws + plan.off_units);
     p.ws.pm = reinterpret_cast<float*>(ws + plan.off_pm);

@@ -69,6 +69,7 @@ struct DecodeWork {
                           //   that record's tile range [lo, hi)}, then the record itself
     int4* seq_info;       // [S] {private tiles per unit, first private tile, first tile
                           //   of its group's shared record (-1: none), group tiles per unit}
+    int* common;          // [S] leading table entries shared with the previous sequence
     int* unit_expect;     // [S * Hkv * nsub] partial states a grouped unit merges
     unsigned* unit_done;  // [S * Hkv * nsub] chunks / segments finished
     float* pm;            // [S * Hq * part_stride]

@@ -76,14 +76,29 @@ cudaError_t launch_decode_mma_nt(const DecodeParams& p, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     DecodeParams ps = p;
     ps.num_workers = occ.ctas[dev];
-    plan_split_kernel<QT><<<1, 1024, 0, stream>>>(ps);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    // the decode (and merge) kernels start launching while their predecessor runs
-    // and wait for it on the device (programmatic dependent launch)
+    // the planner (after the shared-prefix detection of a prefix-aware launch), decode
+    // and merge kernels start launching while their predecessor runs and wait for it
+    // on the device (programmatic dependent launch)
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool grouping = ps.allow_groups && ps.nsub == 1 && ps.group <= kMmaHeadsPerItem;
+    if (grouping) {
+        prefix_common_kernel<QT><<<(unsigned)((ps.num_seqs + 7) / 8), 256, 0, stream>>>(ps);
+        err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(1, 1, 1);
+        pc.blockDim = dim3(1024, 1, 1);
+        pc.stream = stream;
+        pc.attrs = pdl;
+        pc.numAttrs = 1;
+        err = cudaLaunchKernelEx(&pc, plan_split_kernel<QT>, ps);
+    } else {
+        plan_split_kernel<QT><<<1, 1024, 0, stream>>>(ps);
+        err = cudaGetLastError();
+    }
+    if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ps.num_workers, 1, 1);
     cfg.blockDim = dim3(Cfg::THREADS, 1, 1);

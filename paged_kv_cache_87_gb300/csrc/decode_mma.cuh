@@ -114,15 +114,28 @@ struct MmaCfg {
     static constexpr int MTILES = HD / 16;        // mma m-tiles of P.V (over d)
     static constexpr int HALF_BYTES = TPS * 128;  // one 128-byte slice of a stage
     static constexpr int KV_BYTES = HALVES * HALF_BYTES;
-    // the 8-head kernel stages each segment's query rows with its first stage;
-    // the 16-head (prefix) kernel reads them from global memory instead
-    static constexpr int Q_BYTES = NT == 1 ? kMmaHeadsPerItem * HD * 2 : 0;
+    // each segment's query rows (up to 8 heads, or 16 in the prefix kernel) arrive
+    // with its first stage; only the 16-head kernel over 16-bit K/V at head_dim 128,
+    // whose 16 KB stages leave no room, reads them from global memory instead
+    static constexpr bool QSTAGE = NT == 1 || FP8 || HD == 64;
+    static constexpr int Q_BYTES = QSTAGE ? NT * kMmaHeadsPerItem * HD * 2 : 0;
     static constexpr int STAGE_BYTES = (2 * KV_BYTES + Q_BYTES + 1023) / 1024 * 1024;
-    static constexpr int NSTAGE = HD == 128 ? (FP8 ? (NT == 1 ? 5 : 6) : 3) : (NT == 1 ? 5 : 6);
-    static constexpr int THREADS = 64;            // consumer warp + producer warp
+    static constexpr int NSTAGE = HD == 128 ? (FP8 ? (NT == 1 ? 5 : 4) : 3) : (NT == 1 ? 5 : 5);
+    // consumer warps: each takes MTC of a stage's two 16-token m-tiles for all NT
+    // n-tiles; the producer is warp NC.  Two consumers put a CTA at three warps, which
+    // the SM spreads over all four sub-partitions (two-warp CTAs leave the consumers
+    // on two of them).
+    static constexpr int NC = NT;
+    static constexpr int MTC = 2 / NC;
+    static constexpr int THREADS = 32 * (NC + 1);
+    // end of a segment with two consumers: consumer 1 hands its state to consumer 0
+    // one n-tile at a time (per lane: MTILES x 4 accumulators, then m0, m1, l0, l1)
+    static constexpr int XCH_FLOATS = MTILES * 4 + 4;
     static constexpr size_t OFF_METAS = (size_t)NSTAGE * STAGE_BYTES;
     static constexpr size_t OFF_BARS = OFF_METAS + NSTAGE * sizeof(StageMeta);
-    static constexpr size_t SMEM = OFF_BARS + 2 * NSTAGE * sizeof(uint64_t) + 1024;
+    static constexpr size_t OFF_XCH = OFF_BARS + (2 * NSTAGE + 2) * sizeof(uint64_t);
+    static constexpr size_t SMEM =
+        OFF_XCH + (NC > 1 ? (size_t)XCH_FLOATS * 32 * sizeof(float) : 0) + 1024;
     static_assert(HD == 64 || HD == 128, "head_dim");
     static_assert(!FP8 || HD == 128, "FP8 rows must be 128 bytes");
     static_assert(std::is_same<QT, F16>::value || std::is_same<QT, BF16>::value, "q type");
@@ -203,10 +216,60 @@ __device__ __forceinline__ void scan2(int a, int b, int* ex_a, int* ex_b, int* t
 //  4. Per (sequence, unit): the number of partial states its result merges
 //     (shared segments first, then private ones) and where the private ones
 //     start.  Unit counters reset; outputs of empty sequences zeroed.
+// Shared-prefix detection for the prefix-aware decode (one warp per sequence s,
+// many CTAs, before the planner): common[s] = the number of leading block-table
+// entries row s has in common with row s - 1, within the blocks both contexts use
+// (0 for the first sequence of each planner tile of 1024, and whenever either
+// context is empty).  Coalesced loads, 512 entries per round, ballots for the
+// first difference.  Spreading the rows' loads over many SMs keeps the planner's
+// single CTA off this latency-bound work.
+template <typename QT>
+__global__ void __launch_bounds__(256) prefix_common_kernel(DecodeParams p) {
+    pdl_launch_dependents();   // the planner's launch overlaps this kernel
+    const int s = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (s >= p.num_seqs) return;
+    const int B = p.block_size;
+    const int cap = min(p.max_context_len, p.max_blocks * B);
+    auto clamp = [&](int c) { return c < 0 ? 0 : (c > cap ? cap : c); };
+    int common = 0;
+    if (s % 1024 != 0) {
+        const int ca = clamp(__ldg(p.context_lens + s - 1)), cb = clamp(__ldg(p.context_lens + s));
+        const int lim = min((ca + B - 1) / B, (cb + B - 1) / B);
+        const int32_t* ra = p.block_tables + (int64_t)(s - 1) * p.max_blocks;
+        const int32_t* rb = p.block_tables + (int64_t)s * p.max_blocks;
+        common = lim;
+        for (int j0 = 0; j0 < lim; j0 += 512) {
+            bool diff[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int j = j0 + 32 * u + lane;
+                diff[u] = j < lim && __ldg(ra + j) != __ldg(rb + j);
+            }
+            int first = -1;
+#pragma unroll
+            for (int u = 15; u >= 0; --u) {
+                const unsigned m = __ballot_sync(0xffffffffu, diff[u]);
+                if (m) first = j0 + 32 * u + __ffs(m) - 1;
+            }
+            if (first >= 0) {
+                common = first;
+                break;
+            }
+        }
+    }
+    if (lane == 0) p.ws.common[s] = common;
+}
+
+// Record-prefix entries the planner keeps in shared memory for the workers'
+// binary search (larger plans search the global copy).
+constexpr int kPlanSmemRecords = 4096;
+
 template <typename QT>
 __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
     pdl_launch_dependents();   // the decode kernel's prologue overlaps this plan
+    pdl_wait();                // prefix-aware launches: prefix_common_kernel has completed
     __shared__ int s_ctx[1024], s_first[1024], s_run[1024], s_mem[1024], s_sh[1024];
+    __shared__ int s_rp[kPlanSmemRecords + 1];      // record prefix (first tile of each record)
     __shared__ int wa[32], wb[32];
     __shared__ int carry_rec, carry_tiles;
     const int tid = threadIdx.x;
@@ -222,6 +285,9 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         const int s = base + tid;
         const bool valid = s < p.num_seqs;
         int ctx = 0;
+        // entries this sequence's row has in common with its predecessor's (written by
+        // prefix_common_kernel); it loads beside the context length
+        const int common = can_group && valid ? __ldcg(p.ws.common + s) : 0;
         if (valid) {
             ctx = p.context_lens[s];
             if (ctx < 0 || ctx > cap) {
@@ -230,19 +296,13 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
             }
             p.ws.ctx_eff[s] = ctx;
         }
-        const int32_t* row = p.block_tables + (int64_t)s * p.max_blocks;
         s_ctx[tid] = ctx;
-        s_first[tid] = can_group && valid && ctx > 0 ? row[0] : -1 - tid;   // distinct if empty
-        if (can_group && valid && ctx > 0) {
-            // the member compares below read these rows: start them towards L2 now
-            const int nb = (ctx + B - 1) / B;
-            for (int j = 32; j < nb; j += 32) prefetch_l2(row + j);
-            prefetch_l2(row + nb - 1);
-        }
+        s_sh[tid] = common;
         __syncthreads();
-        // run start: inclusive max-scan of (same first block as the previous ? -1 : tid)
-        const bool same = can_group && valid && tid > 0 && s_first[tid] >= 0 &&
-                          s_first[tid] == s_first[tid - 1];
+        // run start: inclusive max-scan of (same first block as the previous ? -1 : tid);
+        // a run never crosses a tile of 1024 sequences
+        const bool same = can_group && valid && tid > 0 && ctx > 0 && s_ctx[tid - 1] > 0 &&
+                          common > 0;
         int run = same ? -1 : tid;
         {
             const int lane = tid & 31, warp = tid >> 5;
@@ -270,42 +330,9 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         // group leaders: every maxm-th position of a run
         const int k = tid - run;
         const bool is_lead = can_group && valid && k % maxm == 0 && ctx > 0;
-        // members: a warp per member compares its table row with its leader's, 128
-        // entries per step (coalesced loads, ballot for the first difference)
-        if (can_group) {
-            const int lane = tid & 31, warp = tid >> 5;
-            const int nvalid = min((int)blockDim.x, p.num_seqs - base);
-            for (int i = warp; i < nvalid; i += blockDim.x >> 5) {
-                const int ki = i - s_run[i];
-                const bool member = ki % maxm != 0 && s_ctx[i] > 0;
-                if (!member) continue;                       // warp-uniform
-                const int lp = i - ki % maxm;
-                const int32_t* ra = p.block_tables + (int64_t)(base + lp) * p.max_blocks;
-                const int32_t* rb = p.block_tables + (int64_t)(base + i) * p.max_blocks;
-                const int lim = min((s_ctx[lp] + B - 1) / B, (s_ctx[i] + B - 1) / B);
-                int common = lim;
-                for (int j0 = 0; j0 < lim; j0 += 512) {
-                    bool diff[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int j = j0 + 32 * u + lane;
-                        diff[u] = j < lim && __ldg(ra + j) != __ldg(rb + j);
-                    }
-                    int first = -1;
-#pragma unroll
-                    for (int u = 15; u >= 0; --u) {
-                        const unsigned m = __ballot_sync(0xffffffffu, diff[u]);
-                        if (m) first = j0 + 32 * u + __ffs(m) - 1;
-                    }
-                    if (first >= 0) {
-                        common = first;
-                        break;
-                    }
-                }
-                if (lane == 0) s_sh[i] = common;             // common leading blocks
-            }
-        }
-        __syncthreads();
+        // a group's shared prefix: the minimum over its members of the entries each has
+        // in common with its predecessor -- equal, by transitivity, to the minimum of
+        // each member's common entries with the leader
         int members = 0, shared = 0;
         if (is_lead) {
             int m = 1;
@@ -346,6 +373,7 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
         if (valid && members >= 2) {
             p.ws.rec[r0] = make_int4(s | kGroupRecord, 0, shared, members);
             p.ws.rec_prefix[r0] = t0;
+            if (r0 < kPlanSmemRecords) s_rp[r0] = t0;
         }
         s_first[tid] = members >= 2 ? t0 : -1;                 // reuse: group tile base
         __syncthreads();
@@ -357,6 +385,7 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
             const int r = r0 + (members >= 2);
             p.ws.rec[r] = make_int4(s, start, ctx, my_gbase);
             p.ws.rec_prefix[r] = pbase;
+            if (r < kPlanSmemRecords) s_rp[r] = pbase;
             p.ws.seq_info[s] = make_int4(priv_tiles, pbase, my_gbase, my_gst);
         }
         __syncthreads();
@@ -376,23 +405,25 @@ __global__ void __launch_bounds__(1024) plan_split_kernel(DecodeParams p) {
     const int q = max(p.chunk_tokens / kTileTokens, (total + p.num_workers - 1) / p.num_workers);
     if (tid == 0) {
         p.ws.rec_prefix[nrec] = total;
+        if (nrec <= kPlanSmemRecords) s_rp[nrec] = total;
         p.ws.quota[0] = q;
         p.ws.quota[1] = total;
     }
     const bool in_smem = p.num_seqs <= (int)blockDim.x;
     __syncthreads();
     // each worker's first record: the last record starting at or before its first
-    // tile (binary search over the record prefix)
+    // tile (binary search over the record prefix, in shared memory when it fits)
+    const int* rp = nrec <= kPlanSmemRecords ? s_rp : p.ws.rec_prefix;
     for (int b = tid; b < p.num_workers; b += blockDim.x) {
         const int pos = b * q;
         if (pos >= total) break;
         int lo = 0, hi = nrec - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (p.ws.rec_prefix[mid] <= pos) lo = mid;
+            if (rp[mid] <= pos) lo = mid;
             else hi = mid - 1;
         }
-        p.ws.worker_first[2 * b] = make_int4(lo, p.ws.rec_prefix[lo], p.ws.rec_prefix[lo + 1], 0);
+        p.ws.worker_first[2 * b] = make_int4(lo, rp[lo], rp[lo + 1], 0);
         p.ws.worker_first[2 * b + 1] = p.ws.rec[lo];
     }
     // sequences without context: zero output (no private and no shared tiles)
@@ -624,7 +655,7 @@ __device__ __forceinline__ void slot_head(const DecodeParams& p, int group, int 
 // --------------------------------------------------------------------- kernel --
 
 template <typename QT, typename KT, int HD, int NT>
-__global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
+__global__ void __launch_bounds__(32 * (NT + 1), 4) decode_mma_kernel(DecodeParams p,
                                                         const __grid_constant__ CUtensorMap tmK,
                                                         const __grid_constant__ CUtensorMap tmV) {
     using Cfg = MmaCfg<QT, KT, HD, NT>;
@@ -636,14 +667,20 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     StageMeta* metas = reinterpret_cast<StageMeta*>(smem + Cfg::OFF_METAS);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BARS);
     uint64_t* empty = full + Cfg::NSTAGE;
+    uint64_t* xfull = empty + Cfg::NSTAGE;    // consumer 1's state is in the exchange buffer
+    uint64_t* xempty = xfull + 1;             // consumer 0 has read it
+    float* xbuf = reinterpret_cast<float*>(smem + Cfg::OFF_XCH);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < Cfg::NSTAGE; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], Cfg::NC);
         }
+        mbar_init(xfull, 1);
+        mbar_init(xempty, 1);
         fence_mbar_init();
+        mbar_arrive(xempty);                  // the buffer starts free (phase 0 complete)
     }
     __syncthreads();
 
@@ -652,7 +689,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     const int q = p.ws.quota[0], total = p.ws.quota[1];   // written by the planning kernel
     const int a = blockIdx.x * q, end = min(a + q, total);
 
-    if (warp == 1) {
+    if (warp == Cfg::NC) {
         // ======================= producer warp =======================
         if (lane == 0) {
             prefetch_tensormap(&tmK);
@@ -701,7 +738,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 }
                 uint8_t* sbase = smem + (size_t)stage * Cfg::STAGE_BYTES;
                 const int fb = ts / B, nblk = (te - 1) / B - fb + 1;   // whole blocks
-                const uint32_t qbytes = NT == 1 && first ? (uint32_t)(win.nh * HD * 2) : 0u;
+                const uint32_t qbytes = Cfg::QSTAGE && first ? (uint32_t)(win.nh * HD * 2) : 0u;
                 if (lane == 0) {
                     StageMeta& m = metas[stage];
                     m.s = win.s; m.kvh = win.kvh; m.qsub = win.qsub; m.nh = win.nh;
@@ -729,11 +766,23 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                                     &tmV, x, y, &full[stage], policy);
                     }
                 }
-                if (qbytes && lane == 31) {
-                    const int h0 = win.kvh * p.group + win.qsub * kMmaHeadsPerItem;
-                    const int64_t qoff = ((int64_t)win.s * p.num_q_heads + h0) * HD * 2;
-                    bulk_g2s(sbase + 2 * Cfg::KV_BYTES, (const uint8_t*)p.q + qoff, qbytes,
-                             &full[stage]);
+                if (qbytes) {
+                    // the segment's query rows in head-slot order: a private unit's heads
+                    // are one contiguous run; a group's are G rows of each member
+                    if (win.group) {
+                        if (lane < win.members) {
+                            const int64_t qoff =
+                                ((int64_t)(win.s + lane) * p.num_q_heads + win.kvh * p.group) * HD * 2;
+                            bulk_g2s(sbase + 2 * Cfg::KV_BYTES + lane * p.group * HD * 2,
+                                     (const uint8_t*)p.q + qoff, (uint32_t)(p.group * HD * 2),
+                                     &full[stage]);
+                        }
+                    } else if (lane == 31) {
+                        const int h0 = win.kvh * p.group + win.qsub * kMmaHeadsPerItem;
+                        const int64_t qoff = ((int64_t)win.s * p.num_q_heads + h0) * HD * 2;
+                        bulk_g2s(sbase + 2 * Cfg::KV_BYTES, (const uint8_t*)p.q + qoff, qbytes,
+                                 &full[stage]);
+                    }
                 }
                 if (++stage == Cfg::NSTAGE) { stage = 0; phase ^= 1u; }
                 if (st == 0) {
@@ -766,7 +815,13 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         return;
     }
 
-    // ========================= consumer warp =========================
+    // ========================= consumer warps =========================
+    // Consumer cw takes m-tiles cw*MTC .. cw*MTC+MTC-1 (16 tokens each) of every stage
+    // for all n-tiles, with its own running state; with two consumers, consumer 1
+    // hands its state to consumer 0 at the end of each segment and consumer 0 merges
+    // the two (the rescale of the running-max recurrence) and finishes the segment.
+    constexpr int MTC = Cfg::MTC;
+    const int cw = warp;
     const bool grp_launch = p.allow_groups != 0;   // merges left to the merge kernel
     const int g = lane >> 2, c = lane & 3;
     uint32_t qf[NT][Cfg::KSTEPS][2];   // Q^T B fragments, n-tile nt = head slots 8nt..8nt+7
@@ -774,14 +829,16 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
     float m0[NT], m1[NT], l0[NT], l1[NT];
     int stage = 0;
     uint32_t phase = 0;
+    uint32_t xphase = 0;               // exchange barrier parity (each consumer its own)
     int nt_live = 1;
+    bool ok = true;
     // d index of C-fragment row g (half 0) or g + 8 (half 1) of P.V m-tile mt
     auto d_row = [&](int mt, int half) -> int {
         if constexpr (Cfg::FP8) return 32 * (mt >> 1) + 2 * g + (mt & 1) + 16 * half;
         else return 16 * mt + g + 8 * half;
     };
 
-    while (true) {
+    while (ok) {
         if (!mbar_wait(&full[stage], phase)) {
             set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
             break;
@@ -793,10 +850,10 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         const uint32_t sV = sK + Cfg::KV_BYTES;
 
         if (meta.flags & kFirst) {
-            // Q^T fragments: from the stage (8-head kernel, rows staged by the producer)
-            // or straight from global memory (16-head kernel; small and L2-resident)
+            // Q^T fragments: from the stage (rows staged by the producer) or, in the
+            // 16-head kernel over 16-bit K/V at head_dim 128, from global memory
             const uint32_t* qg = static_cast<const uint32_t*>(p.q);
-            if constexpr (NT == 1) qg = reinterpret_cast<const uint32_t*>(sbase + 2 * Cfg::KV_BYTES);
+            if constexpr (Cfg::QSTAGE) qg = reinterpret_cast<const uint32_t*>(sbase + 2 * Cfg::KV_BYTES);
             nt_live = meta.nh > 8 ? 2 : 1;
             const bool grp = (meta.flags & kGroup) != 0;
 #pragma unroll
@@ -805,8 +862,8 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 const bool live = hs < meta.nh;
                 int seq = 0, qh = 0;
                 slot_head(p, grp, meta.s, meta.kvh, meta.qsub, live ? hs : 0, &seq, &qh);
-                const int64_t rowq = NT == 1 ? (int64_t)hs * HD                     // staged rows
-                                             : ((int64_t)seq * p.num_q_heads + qh) * HD;
+                const int64_t rowq = Cfg::QSTAGE ? (int64_t)hs * HD                  // staged rows
+                                                 : ((int64_t)seq * p.num_q_heads + qh) * HD;
 #pragma unroll
                 for (int t = 0; t < Cfg::KSTEPS; ++t) {
                     if constexpr (Cfg::FP8) {
@@ -827,9 +884,12 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
         }
 
         const int nvalid = meta.te - meta.ts;            // 1..32
-        if (nvalid < TPS) {
-            // rows past the context: stale or poisoned -> zero V (P is 0 there)
-            const int zrows = TPS - nvalid;
+        const int r_lo = cw * MTC * 16;                  // this consumer's stage rows
+        const int r_hi = r_lo + MTC * 16;
+        const bool mine = nvalid > r_lo;                 // its m-tiles hold tokens
+        if (mine && nvalid < r_hi) {
+            // its rows past the context: stale or poisoned -> zero V (P is 0 there)
+            const int zrows = r_hi - nvalid;
             for (int i = lane; i < zrows * Cfg::HALVES * 8; i += 32) {
                 const int r = nvalid + i / (Cfg::HALVES * 8);
                 const int h = (i / 8) % Cfg::HALVES, ch = i % 8;
@@ -839,15 +899,15 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
             fence_proxy_async_smem();
             __syncwarp();
         }
-        const bool two = nvalid > 16;                    // second m-tile holds tokens
-        // ---- S^T = K . Q^T: (up to) two 16-token m-tiles x (up to) NT 8-head n-tiles ----
-        float sa[2][NT][4];
+        if (mine) {
+        // ---- S^T = K . Q^T: this consumer's (up to) MTC 16-token m-tiles x NT n-tiles ----
+        float sa[MTC][NT][4];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int mi = 0; mi < MTC; ++mi)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sa[mt][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) sa[mi][nt][e] = 0.f;
         {
             const int rl = (lane & 7) + ((lane >> 3) & 1) * 8;
             if constexpr (Cfg::FP8) {
@@ -855,8 +915,9 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 for (int pr = 0; pr < Cfg::KSTEPS / 2; ++pr) {
                     const int chunk = 2 * pr + (lane >> 4);
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        if (mt == 1 && !two) break;
+                    for (int mi = 0; mi < MTC; ++mi) {
+                        const int mt = cw * MTC + mi;
+                        if (mi > 0 && mt * 16 >= nvalid) break;
                         uint32_t r[4];
                         ldsm_x4(sK + swz(16 * mt + rl, chunk), r);
 #pragma unroll
@@ -869,7 +930,7 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt)
                                 if (NT == 1 || nt < nt_live)
-                                    Mma<MT>::run(sa[mt][nt], a, qf[nt][2 * pr + k][0],
+                                    Mma<MT>::run(sa[mi][nt], a, qf[nt][2 * pr + k][0],
                                                  qf[nt][2 * pr + k][1]);
                         }
                     }
@@ -880,33 +941,40 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                     const int half = t >> 2, chunk = (t & 3) * 2 + (lane >> 4);
                     const uint32_t base = sK + half * Cfg::HALF_BYTES;
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        if (mt == 1 && !two) break;
+                    for (int mi = 0; mi < MTC; ++mi) {
+                        const int mt = cw * MTC + mi;
+                        if (mi > 0 && mt * 16 >= nvalid) break;
                         uint32_t a[4];
                         ldsm_x4(base + swz(16 * mt + rl, chunk), a);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
-                            if (NT == 1 || nt < nt_live) Mma<MT>::run(sa[mt][nt], a, qf[nt][t][0], qf[nt][t][1]);
+                            if (NT == 1 || nt < nt_live) Mma<MT>::run(sa[mi][nt], a, qf[nt][t][0], qf[nt][t][1]);
                     }
                 }
             }
         }
         // ---- online softmax over the stage's tokens, per n-tile ----
-        uint32_t pb[2][NT][2];   // P^T B fragments: k-step (tokens 0-15 / 16-31) x n-tile
+        uint32_t pb[MTC][NT][2];   // P^T B fragments: k-step (this consumer's m-tiles) x n-tile
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             if (NT > 1 && nt >= nt_live) break;
-            float x[2][4];
+            float x[MTC][4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mi = 0; mi < MTC; ++mi) {
+                const int mt = cw * MTC + mi;
                 const bool va = mt * 16 + g < nvalid, vb = mt * 16 + g + 8 < nvalid;
-                x[mt][0] = va ? sa[mt][nt][0] * p.qk_scale_log2 : -INFINITY;
-                x[mt][1] = va ? sa[mt][nt][1] * p.qk_scale_log2 : -INFINITY;
-                x[mt][2] = vb ? sa[mt][nt][2] * p.qk_scale_log2 : -INFINITY;
-                x[mt][3] = vb ? sa[mt][nt][3] * p.qk_scale_log2 : -INFINITY;
+                x[mi][0] = va ? sa[mi][nt][0] * p.qk_scale_log2 : -INFINITY;
+                x[mi][1] = va ? sa[mi][nt][1] * p.qk_scale_log2 : -INFINITY;
+                x[mi][2] = vb ? sa[mi][nt][2] * p.qk_scale_log2 : -INFINITY;
+                x[mi][3] = vb ? sa[mi][nt][3] * p.qk_scale_log2 : -INFINITY;
             }
-            float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
-            float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+            float mx0 = fmaxf(x[0][0], x[0][2]);
+            float mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+            for (int mi = 1; mi < MTC; ++mi) {
+                mx0 = fmaxf(mx0, fmaxf(x[mi][0], x[mi][2]));
+                mx1 = fmaxf(mx1, fmaxf(x[mi][1], x[mi][3]));
+            }
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -929,29 +997,30 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 }
             }
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int mi = 0; mi < MTC; ++mi) {
                 float f0, f1, f2, f3;
-                const uint32_t p01 = Mma<MT>::pack(fast_exp2(x[mt][0] - m0[nt]),
-                                                   fast_exp2(x[mt][1] - m1[nt]), f0, f1);
-                const uint32_t p23 = Mma<MT>::pack(fast_exp2(x[mt][2] - m0[nt]),
-                                                   fast_exp2(x[mt][3] - m1[nt]), f2, f3);
+                const uint32_t p01 = Mma<MT>::pack(fast_exp2(x[mi][0] - m0[nt]),
+                                                   fast_exp2(x[mi][1] - m1[nt]), f0, f1);
+                const uint32_t p23 = Mma<MT>::pack(fast_exp2(x[mi][2] - m0[nt]),
+                                                   fast_exp2(x[mi][3] - m1[nt]), f2, f3);
                 l0[nt] += f0 + f2;
                 l1[nt] += f1 + f3;
-                pb[mt][nt][0] = movmatrix_trans(p01);
-                pb[mt][nt][1] = movmatrix_trans(p23);
+                pb[mi][nt][0] = movmatrix_trans(p01);
+                pb[mi][nt][1] = movmatrix_trans(p23);
             }
         }
         // ---- O^T += V^T . P^T ----
         {
-            const int mi = lane >> 3;
-            const int rv = (lane & 7) + (mi >> 1) * 8;
+            const int mi_ = lane >> 3;
+            const int rv = (lane & 7) + (mi_ >> 1) * 8;
             if constexpr (Cfg::FP8) {
 #pragma unroll
                 for (int pr = 0; pr < Cfg::MTILES / 2; ++pr) {
-                    const int chunk = 2 * pr + (mi & 1);
+                    const int chunk = 2 * pr + (mi_ & 1);
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        if (ks == 1 && !two) break;
+                    for (int ki = 0; ki < MTC; ++ki) {
+                        const int ks = cw * MTC + ki;
+                        if (ki > 0 && ks * 16 >= nvalid) break;
                         uint32_t r[4];
                         ldsm_x4_trans(sV + swz(16 * ks + rv, chunk), r);
                         uint32_t ev[4], od[4];
@@ -963,36 +1032,90 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             if (NT > 1 && nt >= nt_live) break;
-                            Mma<MT>::run(o[2 * pr][nt], ev, pb[ks][nt][0], pb[ks][nt][1]);
-                            Mma<MT>::run(o[2 * pr + 1][nt], od, pb[ks][nt][0], pb[ks][nt][1]);
+                            Mma<MT>::run(o[2 * pr][nt], ev, pb[ki][nt][0], pb[ki][nt][1]);
+                            Mma<MT>::run(o[2 * pr + 1][nt], od, pb[ki][nt][0], pb[ki][nt][1]);
                         }
                     }
                 }
             } else {
 #pragma unroll
                 for (int mt = 0; mt < Cfg::MTILES; ++mt) {
-                    const int half = mt >> 2, chunk = (mt & 3) * 2 + (mi & 1);
+                    const int half = mt >> 2, chunk = (mt & 3) * 2 + (mi_ & 1);
                     const uint32_t base = sV + half * Cfg::HALF_BYTES;
 #pragma unroll
-                    for (int ks = 0; ks < 2; ++ks) {
-                        if (ks == 1 && !two) break;
+                    for (int ki = 0; ki < MTC; ++ki) {
+                        const int ks = cw * MTC + ki;
+                        if (ki > 0 && ks * 16 >= nvalid) break;
                         uint32_t a[4];
                         ldsm_x4_trans(base + swz(16 * ks + rv, chunk), a);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt)
                             if (NT == 1 || nt < nt_live)
-                                Mma<MT>::run(o[mt][nt], a, pb[ks][nt][0], pb[ks][nt][1]);
+                                Mma<MT>::run(o[mt][nt], a, pb[ki][nt][0], pb[ki][nt][1]);
                     }
                 }
             }
         }
+        }   // mine
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
         if (++stage == Cfg::NSTAGE) { stage = 0; phase ^= 1u; }
 
         if (!(meta.flags & kLast)) continue;
 
-        // ---------------- end of the segment (warp-local) ----------------
+        // ---------------- end of the segment ----------------
+        if constexpr (Cfg::NC > 1) {
+            // consumer 1 -> consumer 0, one n-tile per round, through the exchange buffer
+            // (lane-interleaved: value i of lane l at xbuf[32 i + l], no bank conflicts)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (nt >= nt_live) break;
+                if (!mbar_wait(cw == 1 ? xempty : xfull, xphase)) {
+                    set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                xphase ^= 1u;
+                if (cw == 1) {
+#pragma unroll
+                    for (int mt = 0; mt < Cfg::MTILES; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) xbuf[32 * (4 * mt + e) + lane] = o[mt][nt][e];
+                    xbuf[32 * (Cfg::MTILES * 4 + 0) + lane] = m0[nt];
+                    xbuf[32 * (Cfg::MTILES * 4 + 1) + lane] = m1[nt];
+                    xbuf[32 * (Cfg::MTILES * 4 + 2) + lane] = l0[nt];
+                    xbuf[32 * (Cfg::MTILES * 4 + 3) + lane] = l1[nt];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xfull);
+                } else {
+                    const float mb0 = xbuf[32 * (Cfg::MTILES * 4 + 0) + lane];
+                    const float mb1 = xbuf[32 * (Cfg::MTILES * 4 + 1) + lane];
+                    const float lb0 = xbuf[32 * (Cfg::MTILES * 4 + 2) + lane];
+                    const float lb1 = xbuf[32 * (Cfg::MTILES * 4 + 3) + lane];
+                    // every lane of a head column holds the same m; a side that saw no
+                    // token of the segment has m = -inf and contributes nothing
+                    const float M0 = fmaxf(m0[nt], mb0), M1 = fmaxf(m1[nt], mb1);
+                    const float ra0 = m0[nt] == -INFINITY ? 0.f : fast_exp2(m0[nt] - M0);
+                    const float rb0 = mb0 == -INFINITY ? 0.f : fast_exp2(mb0 - M0);
+                    const float ra1 = m1[nt] == -INFINITY ? 0.f : fast_exp2(m1[nt] - M1);
+                    const float rb1 = mb1 == -INFINITY ? 0.f : fast_exp2(mb1 - M1);
+#pragma unroll
+                    for (int mt = 0; mt < Cfg::MTILES; ++mt) {
+                        o[mt][nt][0] = o[mt][nt][0] * ra0 + xbuf[32 * (4 * mt + 0) + lane] * rb0;
+                        o[mt][nt][1] = o[mt][nt][1] * ra1 + xbuf[32 * (4 * mt + 1) + lane] * rb1;
+                        o[mt][nt][2] = o[mt][nt][2] * ra0 + xbuf[32 * (4 * mt + 2) + lane] * rb0;
+                        o[mt][nt][3] = o[mt][nt][3] * ra1 + xbuf[32 * (4 * mt + 3) + lane] * rb1;
+                    }
+                    l0[nt] = l0[nt] * ra0 + lb0 * rb0;
+                    l1[nt] = l1[nt] * ra1 + lb1 * rb1;
+                    m0[nt] = M0;
+                    m1[nt] = M1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xempty);
+                }
+            }
+            if (!ok || cw != 0) continue;
+        }
         const bool grp = (meta.flags & kGroup) != 0;
         const int upi = p.num_kv_heads * p.nsub;
 #pragma unroll
@@ -1037,24 +1160,26 @@ __global__ void __launch_bounds__(64, 4) decode_mma_kernel(DecodeParams p,
                 }
             }
         }
-        // split units: lane i (< units served) arrives on unit i's counter once the
-        // warp barrier has ordered every lane's partial-state stores before it;
-        // units the segment covers whole need neither.  Grouped launches leave
-        // every merge to the merge kernel.
-        __syncwarp();
-        if (grp_launch) continue;
-        const int my_expect = meta.expect;
-        bool last = false;
-        if (lane == 0 && my_expect > 1) {
-            const int unit = meta.s * upi + meta.kvh * p.nsub + meta.qsub;
-            last = atom_add_acq_rel_gpu(&p.ws.unit_done[unit], 1u) == (unsigned)(my_expect - 1);
+        if constexpr (Cfg::NC == 1) {
+            // split units: lane i (< units served) arrives on unit i's counter once the
+            // warp barrier has ordered every lane's partial-state stores before it;
+            // units the segment covers whole need neither.  Grouped launches leave
+            // every merge to the merge kernel (the two-consumer kernel serves only those).
+            __syncwarp();
+            if (grp_launch) continue;
+            const int my_expect = meta.expect;
+            bool last = false;
+            if (lane == 0 && my_expect > 1) {
+                const int unit = meta.s * upi + meta.kvh * p.nsub + meta.qsub;
+                last = atom_add_acq_rel_gpu(&p.ws.unit_done[unit], 1u) == (unsigned)(my_expect - 1);
+            }
+            unsigned last_mask = __ballot_sync(0xffffffffu, last);
+            if (last_mask) __syncwarp();   // the acquiring lane's view reaches the warp
+            // the merge of the unit this warp finished last
+            if (last_mask)
+                merge_unit_warp<QT, HD>(p, (int64_t)meta.s * p.num_q_heads + meta.kvh * p.group +
+                                               meta.qsub * kMmaHeadsPerItem, meta.nh, my_expect, lane);
         }
-        unsigned last_mask = __ballot_sync(0xffffffffu, last);
-        if (last_mask) __syncwarp();   // the acquiring lane's view reaches the warp
-        // the merge of the unit this warp finished last
-        if (last_mask)
-            merge_unit_warp<QT, HD>(p, (int64_t)meta.s * p.num_q_heads + meta.kvh * p.group +
-                                           meta.qsub * kMmaHeadsPerItem, meta.nh, my_expect, lane);
     }
 }
 

@@ -139,10 +139,14 @@ def test_per_config_entry_uses_unique_bytes_for_the_roofline():
 def test_launch_count_per_step():
     from types import SimpleNamespace
     import numpy as np
-    w = SimpleNamespace(q_dtype="bf16", kv_dtype="e4m3", head_dim=128,
-                        step_pairs=np.zeros((32, 2), np.int32))
-    assert bench.launches_per_step(w, True) == 5       # copy, append, plan, decode, merge
+    w = SimpleNamespace(q_dtype="bf16", kv_dtype="e4m3", head_dim=128, num_q_heads=32,
+                        num_kv_heads=8, step_pairs=np.zeros((32, 2), np.int32))
+    # copy, append, shared-prefix detection, plan, decode, merge
+    assert bench.launches_per_step(w, True) == 6
     assert bench.launches_per_step(w, False) == 4
+    w.num_q_heads = 128                                # 16 heads per kv head: no groups
+    assert bench.launches_per_step(w, True) == 4
+    w.num_q_heads = 32
     w.step_pairs = np.zeros((0, 2), np.int32)
     w.q_dtype, w.kv_dtype = "f32", "f32"
     assert bench.launches_per_step(w, True) == 3       # append, plan, decode (CUDA cores)

@@ -114,3 +114,39 @@ def test_plain_batch_above_one_planner_tile():
                                 scale=1 / math.sqrt(64))
     st = _check(w, prefix=False)
     assert (st.out_f64()[ctx == 0] == 0).all()
+
+
+def _prefix_workload(seed, B=16, groups=3, lo=600, hi=900):
+    rng = np.random.default_rng(seed)
+    return inputs.make_shared_prefix("prefix", rng, num_groups=groups, samples=4, prefix_lo=lo,
+                                     prefix_hi=hi, tail_lo=1, tail_hi=60, num_q_heads=16,
+                                     num_kv_heads=4, head_dim=128, block_size=B, q_dtype="bf16",
+                                     kv_dtype="bf16", kv_scale=1.0, scale=1 / math.sqrt(128))
+
+
+@pytest.mark.parametrize("pad", [0, 1, 2, 3])
+def test_table_width_of_every_alignment(pad):
+    """Tables whose rows start at every 4-byte offset modulo 16 (padded widths)."""
+    import dataclasses
+    w = _prefix_workload(31)
+    width = (w.max_blocks + 3) // 4 * 4 + pad
+    t = np.full((w.num_seqs, width), -1, np.int32)
+    t[:, :w.max_blocks] = w.block_tables
+    _check(dataclasses.replace(w, block_tables=t))
+
+
+@pytest.mark.parametrize("pad", [0, 1])
+def test_member_rows_that_diverge_inside_the_prefix(pad):
+    """Members whose rows leave the leader's at entries 5, 100 and 140 (the planner
+    compares rows in spans of 128 entries): only the entries before the first
+    difference are shared."""
+    import dataclasses
+    w = _prefix_workload(32, lo=2500, hi=3000)
+    width = (w.max_blocks + 3) // 4 * 4 + pad
+    t = np.full((w.num_seqs, width), -1, np.int32)
+    t[:, :w.max_blocks] = w.block_tables
+    donor = int(t[8, 1])                     # a full block of another group's prompt
+    for seq, j in ((1, 5), (2, 100), (3, 140)):
+        assert t[seq, j] != donor and j * 16 + 16 <= w.context_lens[seq] - 64
+        t[seq, j] = donor
+    _check(dataclasses.replace(w, block_tables=t))
