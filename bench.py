@@ -322,10 +322,14 @@ def time_decode_steps(torch, st, stream, steps, warmup, flush_buf, world=1, devi
     Returns (step ms, decode ms) per timed step; the decode events bracket the
     decode call alone (planning + decode (+ merge) kernels).  `flush_buf`, when
     given, is written before every timed step (outside the events) so the step
-    starts with a cold L2."""
+    starts with a cold L2.  The step's calls are prepared once (arguments
+    marshalled), so the host issues each launch with one ctypes call."""
+    pre, dec = st.prepare(stream)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            st.step(stream)
+            for c in pre:
+                c()
+            dec()
         stream.synchronize()
         barrier(world)
         torch.cuda.synchronize(device)
@@ -335,10 +339,10 @@ def time_decode_steps(torch, st, stream, steps, warmup, flush_buf, world=1, devi
                 flush_buf.zero_()
             s0, d0, d1, s1 = ev[i]
             s0.record(stream)
-            st.copy_step(stream)
-            st.append_step(stream)
+            for c in pre:
+                c()
             d0.record(stream)
-            st.decode(stream)
+            dec()
             d1.record(stream)
             s1.record(stream)
         stream.synchronize()
@@ -421,6 +425,7 @@ def run_ours(args, rank, world, local):
     h_in, d_in = st.pack_step_inputs()
     h_out = torch.empty_like(st.out, device="cpu").pin_memory()
     h2d, d2h = h_in.numel(), h_out.numel() * h_out.element_size()
+    pre, dec = st.prepare(stream)                 # the inputs moved: marshal again
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
@@ -429,7 +434,9 @@ def run_ours(args, rank, world, local):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             d_in.copy_(h_in, non_blocking=True)
-            st.step(stream)
+            for c in pre:
+                c()
+            dec()
             h_out.copy_(st.out, non_blocking=True)
             b.record(stream)
             b.synchronize()
@@ -761,7 +768,12 @@ def run_reference(args, rank, world, local):
 
 
 def run_swap(args, rank, world, local):
-    """Swap bandwidth: the workload's used blocks out to pinned host memory and back."""
+    """Swap bandwidth: the workload's used blocks out to pinned host memory and back.
+
+    Beside pkv_swap_blocks, the same number of bytes is moved in the same run by plain
+    cudaMemcpyAsync calls (one per pool and direction, between a contiguous device
+    range and the pinned pool): the host link's copy-engine rate, which the kernel's
+    fraction is reported against."""
     import torch
     from paged_kv_cache_87_gb300 import binding, build, inputs
     from paged_kv_cache_87_gb300.session import DeviceState
@@ -779,25 +791,40 @@ def run_swap(args, rank, world, local):
     in_pairs = torch.from_numpy(np.stack([np.arange(len(used)), used], 1).astype(np.int32)
                                 ).cuda()
     nbytes = 2 * len(used) * st.k_cache[0].numel() * st.k_cache.element_size()
+    dk, dv = st.k_cache[:len(used)], st.v_cache[:len(used)]   # contiguous device ranges
     stream = torch.cuda.Stream()
-    res = {}
-    with torch.cuda.stream(stream):
-        for name, args_ in (("swap_out_gbs", (st.k_cache, st.v_cache, hk, hv, out_pairs)),
-                            ("swap_in_gbs", (hk, hv, st.k_cache, st.v_cache, in_pairs))):
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
             for _ in range(args.warmup):
-                binding.pkv_swap_blocks(*args_, stream=stream)
+                fn()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for _ in range(args.steps):
-                binding.pkv_swap_blocks(*args_, stream=stream)
+                fn()
             e1.record(stream)
             e1.synchronize()
-            res[name] = round(nbytes * args.steps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        return round(nbytes * args.steps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+
+    res = {}
+    res["swap_out_gbs"] = timed(lambda: binding.pkv_swap_blocks(
+        st.k_cache, st.v_cache, hk, hv, out_pairs, stream=stream))
+    res["swap_in_gbs"] = timed(lambda: binding.pkv_swap_blocks(
+        hk, hv, st.k_cache, st.v_cache, in_pairs, stream=stream))
     assert binding.pkv_get_device_status() == 0
+    res["memcpy_d2h_gbs"] = timed(lambda: (hk.copy_(dk, non_blocking=True),
+                                           hv.copy_(dv, non_blocking=True)))
+    res["memcpy_h2d_gbs"] = timed(lambda: (dk.copy_(hk, non_blocking=True),
+                                           dv.copy_(hv, non_blocking=True)))
+    res["frac_out"] = round(res["swap_out_gbs"] / res["memcpy_d2h_gbs"], 4)
+    res["frac_in"] = round(res["swap_in_gbs"] / res["memcpy_h2d_gbs"], 4)
     if rank == 0:
         print(json.dumps({"metric": "pkv_swap_blocks bandwidth (device pool <-> pinned host)",
                           "unit": "GB/s", **res, "bytes_per_call": nbytes,
                           "blocks": int(len(used)), "steps": args.steps,
+                          "peak": {"out": res["memcpy_d2h_gbs"], "in": res["memcpy_h2d_gbs"],
+                                   "source": "same-run cudaMemcpyAsync of the same bytes "
+                                             "(contiguous device range <-> pinned pool)"},
                           "config": {"workload": w.name}}), flush=True)
 
 

@@ -169,20 +169,9 @@ def pkv_decode_workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: in
                                                  dtype_code(kv_dtype)))
 
 
-def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                               block_tables: torch.Tensor, context_lens: torch.Tensor,
-                               max_context_len: int, scale: float, kv_scale: float = 1.0,
-                               workspace: torch.Tensor | None = None,
-                               out: torch.Tensor | None = None, stream=None,
-                               prefix: bool = False) -> torch.Tensor:
-    """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s over context_lens[s] tokens.
-
-    query [S, Hq, d]; k_cache / v_cache [NB, Hkv, B, d] (float8_e4m3fn or uint8
-    for FP8); block_tables int32 [S, max_blocks]; context_lens int32 [S].
-    ``workspace`` (uint8, >= pkv_decode_workspace_bytes) is allocated if None.
-    ``prefix=True`` calls pkv_paged_decode_attention_prefix (shared prompts
-    read once per group of sequences).
-    """
+def _decode_args(query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+                 kv_scale, workspace, out, stream, prefix):
+    """Checks and marshals a decode call: (C function name, argument tuple, out, workspace)."""
     S, Hq, d = query.shape
     NB, Hkv, B, d2 = k_cache.shape
     if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape):
@@ -201,13 +190,63 @@ def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cac
     _cuda(out, "out")
     _cuda(workspace, "workspace")
     fn = "pkv_paged_decode_attention_prefix" if prefix else "pkv_paged_decode_attention"
-    st = getattr(load(), fn)(
-        query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), S, Hq, Hkv, d, B, NB, block_tables.shape[1],
-        int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
-    _check(fn, st)
+    args = (query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), S, Hq, Hkv, d, B, NB, block_tables.shape[1],
+            int(max_context_len), float(scale), qc, kc, float(kv_scale), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), out.data_ptr(), _stream_ptr(stream))
+    return fn, args, out, workspace
+
+
+def pkv_paged_decode_attention(query: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               max_context_len: int, scale: float, kv_scale: float = 1.0,
+                               workspace: torch.Tensor | None = None,
+                               out: torch.Tensor | None = None, stream=None,
+                               prefix: bool = False) -> torch.Tensor:
+    """out[s, h] = softmax(scale * q[s, h] . K_s^T) V_s over context_lens[s] tokens.
+
+    query [S, Hq, d]; k_cache / v_cache [NB, Hkv, B, d] (float8_e4m3fn or uint8
+    for FP8); block_tables int32 [S, max_blocks]; context_lens int32 [S].
+    ``workspace`` (uint8, >= pkv_decode_workspace_bytes) is allocated if None.
+    ``prefix=True`` calls pkv_paged_decode_attention_prefix (shared prompts
+    read once per group of sequences).
+    """
+    fn, args, out, _ = _decode_args(query, k_cache, v_cache, block_tables, context_lens,
+                                    max_context_len, scale, kv_scale, workspace, out, stream,
+                                    prefix)
+    _check(fn, getattr(load(), fn)(*args))
     return out
+
+
+class PreparedCall:
+    """One C-ABI call whose arguments (pointers, sizes, stream) were checked and
+    marshalled once; calling it issues the same call again.
+
+    For a serving loop that runs the same step on the same buffers every
+    iteration: the per-call Python cost drops to one ctypes call.  The tensors
+    behind the pointers are kept referenced here and must not be reallocated."""
+
+    def __init__(self, name: str, args: tuple, keep: tuple = ()):
+        self.name = name
+        self._fn = getattr(load(), name)
+        self._args = tuple(args)
+        self._keep = keep
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != PKV_OK:
+            raise PagedKVError(self.name, st)
+
+
+def prepare_paged_decode_attention(query, k_cache, v_cache, block_tables, context_lens,
+                                   max_context_len, scale, kv_scale=1.0, workspace=None,
+                                   out=None, stream=None, prefix=False) -> PreparedCall:
+    """pkv_paged_decode_attention (or the prefix-aware entry) as a PreparedCall."""
+    fn, args, out, workspace = _decode_args(query, k_cache, v_cache, block_tables,
+                                            context_lens, max_context_len, scale, kv_scale,
+                                            workspace, out, stream, prefix)
+    return PreparedCall(fn, args, (query, k_cache, v_cache, block_tables, context_lens,
+                                   workspace, out))
 
 
 def pkv_multi_query_workspace_bytes(num_seqs: int) -> int:
@@ -322,10 +361,7 @@ def pkv_paged_decode_attention_noalloc(query: torch.Tensor, k_cache: torch.Tenso
     return out
 
 
-def pkv_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
-                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
-                          kv_scale: float = 1.0, stream=None) -> None:
-    """k_cache[slot // B, h, slot % B] = key[t, h] (e4m3(x / kv_scale) for FP8 caches)."""
+def _reshape_args(key, value, k_cache, v_cache, slot_mapping, kv_scale, stream):
     T, Hkv, d = key.shape
     NB, Hkv2, B, d2 = k_cache.shape
     if (Hkv2, d2) != (Hkv, d) or tuple(value.shape) != tuple(key.shape):
@@ -335,11 +371,25 @@ def pkv_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch
     for t, n in ((key, "key"), (value, "value"), (k_cache, "k_cache"), (v_cache, "v_cache"),
                  (slot_mapping, "slot_mapping")):
         _cuda(t, n)
-    st = load().pkv_reshape_and_cache(
-        key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-        slot_mapping.data_ptr(), T, Hkv, d, B, NB, dtype_code(key), dtype_code(k_cache),
-        float(kv_scale), _stream_ptr(stream))
-    _check("pkv_reshape_and_cache", st)
+    return (key.data_ptr(), value.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+            slot_mapping.data_ptr(), T, Hkv, d, B, NB, dtype_code(key), dtype_code(k_cache),
+            float(kv_scale), _stream_ptr(stream))
+
+
+def pkv_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                          kv_scale: float = 1.0, stream=None) -> None:
+    """k_cache[slot // B, h, slot % B] = key[t, h] (e4m3(x / kv_scale) for FP8 caches)."""
+    args = _reshape_args(key, value, k_cache, v_cache, slot_mapping, kv_scale, stream)
+    _check("pkv_reshape_and_cache", load().pkv_reshape_and_cache(*args))
+
+
+def prepare_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, kv_scale=1.0,
+                              stream=None) -> PreparedCall:
+    """pkv_reshape_and_cache as a PreparedCall."""
+    return PreparedCall("pkv_reshape_and_cache",
+                        _reshape_args(key, value, k_cache, v_cache, slot_mapping, kv_scale,
+                                      stream), (key, value, k_cache, v_cache, slot_mapping))
 
 
 def validate_pairs(pairs: np.ndarray, num_blocks: int) -> None:
@@ -354,14 +404,7 @@ def validate_pairs(pairs: np.ndarray, num_blocks: int) -> None:
         raise ValueError("copy_blocks: a destination block is also a source")
 
 
-def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
-                    stream=None) -> None:
-    """Copy physical blocks src -> dst of both caches for every (src, dst) pair.
-
-    ``src_dst_pairs``: int32 [n, 2].  A host array/tensor is validated and
-    copied to the device; a CUDA tensor is used as is (the caller has
-    validated it).
-    """
+def _copy_args(k_cache, v_cache, src_dst_pairs, stream):
     NB, Hkv, B, d = k_cache.shape
     _cuda(k_cache, "k_cache")
     _cuda(v_cache, "v_cache")
@@ -374,10 +417,26 @@ def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
     if pairs.dtype != torch.int32:
         raise ValueError("src_dst_pairs must be int32")
     n = pairs.numel() // 2
-    st = load().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
-                                pairs.data_ptr() if n else None, n, Hkv, d, B, NB,
-                                dtype_code(k_cache), _stream_ptr(stream))
-    _check("pkv_copy_blocks", st)
+    return (k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr() if n else None, n, Hkv, d,
+            B, NB, dtype_code(k_cache), _stream_ptr(stream)), pairs
+
+
+def pkv_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs,
+                    stream=None) -> None:
+    """Copy physical blocks src -> dst of both caches for every (src, dst) pair.
+
+    ``src_dst_pairs``: int32 [n, 2].  A host array/tensor is validated and
+    copied to the device; a CUDA tensor is used as is (the caller has
+    validated it).
+    """
+    args, _ = _copy_args(k_cache, v_cache, src_dst_pairs, stream)
+    _check("pkv_copy_blocks", load().pkv_copy_blocks(*args))
+
+
+def prepare_copy_blocks(k_cache, v_cache, src_dst_pairs, stream=None) -> PreparedCall:
+    """pkv_copy_blocks as a PreparedCall (device pairs are used as they are then)."""
+    args, pairs = _copy_args(k_cache, v_cache, src_dst_pairs, stream)
+    return PreparedCall("pkv_copy_blocks", args, (k_cache, v_cache, pairs))
 
 
 def pkv_swap_blocks(src_k: torch.Tensor, src_v: torch.Tensor, dst_k: torch.Tensor,

@@ -215,6 +215,9 @@ pkv_status decode_impl(const void* query, const void* k_cache, const void* v_cac
                      (int64_t)num_blocks * num_kv_heads * block_size <= 0x7fffffffLL;
     const int hpi = mma ? kMmaHeadsPerItem : plan.hpi;
     p.nsub = (plan.group + hpi - 1) / hpi;   // never above plan.nsub: the workspace fits
+    // CUDA-core path with every context within one chunk: no split, no merge, so the
+    // decode kernel takes its work items straight from the sequence index (one launch)
+    p.self_plan = !mma && max_context_len <= plan.chunk_tokens;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (q_dtype) {

@@ -48,6 +48,7 @@ __device__ __forceinline__ void load16_as_float<BF16>(const uint8_t* src, float*
 // One thread = one 16-byte chunk of one (token, kv head) row of the cache.
 template <typename ST, bool QUANT>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(ReshapeParams p) {
+    pdl_launch_dependents();   // the decode launched next may start its launch now
     constexpr int KB = QUANT ? 1 : ST::bytes;          // cache element bytes
     const int row_chunks = p.head_dim * KB / 16;
     const int64_t total = (int64_t)p.num_tokens * p.num_kv_heads * row_chunks;
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(ReshapeParams p)
 // grid = (pairs, slices of a block, 2 caches); one 16-byte chunk per thread-iteration.
 // Block pairs[i][0] of the source pool -> block pairs[i][1] of the destination.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(CopyParams p) {
+    pdl_launch_dependents();
     const int pair = blockIdx.x;
     const int32_t src = p.pairs[2 * pair], dst = p.pairs[2 * pair + 1];
     if (src < 0 || src >= p.src_num_blocks || dst < 0 || dst >= p.dst_num_blocks) {

@@ -51,6 +51,15 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) {
 
 // ------------------------------------------------------------- mbarrier --
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel on its stream still runs;
+// pdl_wait blocks until that kernel has completed and its memory is visible.
+// pdl_launch_dependents lets the next such kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                  : "memory");

@@ -45,15 +45,6 @@ constexpr int kGroupRecord = 1 << 30;  // record code flag: a shared-prefix grou
 constexpr int kMaxGroupHeads = 16;     // query heads a shared-prefix unit serves
 constexpr int kTileTokens = 64;        // split granularity of the balanced split
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialisation may start while the previous kernel on its stream still runs;
-// pdl_wait blocks until that kernel has completed and its memory is visible.
-// pdl_launch_dependents lets the next such kernel start launching.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 struct DecodeWork {
     unsigned* counter;    // next work index (dynamic items)
     unsigned* total;      // number of work indices (dynamic items)
@@ -93,6 +84,8 @@ struct DecodeParams {
     int num_workers;      // CTAs of the balanced-split decode
     int allow_groups;     // group sequences that share leading blocks (prefix-aware decode);
                           // its split units are merged by a separate merge kernel
+    int self_plan;        // CUDA-core path, every context within one chunk: no planning
+                          // kernel; work item w is (sequence w / units, unit w % units)
     float qk_scale_log2;  // scale * log2(e) (* kv_scale for FP8)
     float out_scale;      // kv_scale for FP8, else 1
 };
@@ -101,6 +94,7 @@ struct DecodeParams {
 
 template <typename QT>
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeParams p) {
+    pdl_launch_dependents();   // the decode kernel's launch overlaps this plan
     __shared__ int warp_sums[32];
     __shared__ int carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -336,34 +330,65 @@ __global__ void __launch_bounds__(SimtCfg<QT, KT, HD, HPI>::THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();   // the preceding kernel (planner, or the cache write) has completed
 
-    const unsigned total = *p.ws.total;
     const int B = p.block_size, C = p.chunk_tokens;
     const int units_per_item = p.num_kv_heads * p.nsub;
+    const unsigned total = p.self_plan ? (unsigned)(p.num_seqs * units_per_item) : *p.ws.total;
 
     if (warp == Cfg::NCW) {
         // ======================= producer warp =======================
         const uint64_t policy = l2_evict_first_policy();
         int stage = 0;
         uint32_t phase = 0;
-        unsigned w = 0;
-        if (lane == 0) w = atomicAdd(p.ws.counter, 1u);
-        w = __shfl_sync(0xffffffffu, w, 0);
+        unsigned w = blockIdx.x;
+        if (!p.self_plan) {
+            if (lane == 0) w = atomicAdd(p.ws.counter, 1u);
+            w = __shfl_sync(0xffffffffu, w, 0);
+        }
         bool ok = true;
         while (w < total && ok) {
-            unsigned wn = 0;
-            if (lane == 0) wn = atomicAdd(p.ws.counter, 1u);   // overlaps the item below
+            unsigned wn = w + gridDim.x;
+            if (!p.self_plan && lane == 0) wn = atomicAdd(p.ws.counter, 1u);   // overlaps the item
             const int it = (int)(w / units_per_item), rem = (int)(w % units_per_item);
             const int kvh = rem / p.nsub, qsub = rem % p.nsub;
-            const int2 sc = p.ws.items[it];
-            const int s = sc.x, chunk = sc.y;
-            const int ctx = p.ws.ctx_eff[s];
+            int s, chunk, ctx, e0, e1;
+            if (p.self_plan) {
+                // one chunk per sequence: the table's first entries load beside the length
+                s = it;
+                chunk = 0;
+                const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
+                e0 = lane < p.max_blocks ? trow[lane] : 0;
+                e1 = lane + 32 < p.max_blocks ? trow[lane + 32] : 0;
+                ctx = p.context_lens[s];
+                const int cap = min(p.max_context_len, p.max_blocks * B);
+                if (ctx < 0 || ctx > cap) {
+                    if (rem == 0) set_status(p.status, PKV_DEV_BAD_CONTEXT);
+                    ctx = ctx < 0 ? 0 : cap;
+                }
+                if (ctx == 0) {
+                    // no context: this unit's heads of the output are zero
+                    const int h0z = kvh * p.group + qsub * HPI;
+                    const int nhz = min(HPI, p.group - qsub * HPI);
+                    const int64_t o0 = ((int64_t)s * p.num_q_heads + h0z) * HD;
+                    for (int i = lane; i < nhz * HD; i += 32) store_from_float<QT>(p.out, o0 + i, 0.f);
+                    w = wn;
+                    continue;
+                }
+            } else {
+                const int2 sc = p.ws.items[it];
+                s = sc.x;
+                chunk = sc.y;
+                ctx = p.ws.ctx_eff[s];
+            }
             const int nchunks = (ctx + C - 1) / C;
             const int t0 = chunk * C, t1 = min(t0 + C, ctx);
             const int jb0 = t0 / B, nb = (t1 + B - 1) / B - jb0;
-            const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
-            int e0 = lane < nb ? trow[jb0 + lane] : 0;
-            int e1 = lane + 32 < nb ? trow[jb0 + lane + 32] : 0;
+            if (!p.self_plan) {
+                const int32_t* trow = p.block_tables + (int64_t)s * p.max_blocks;
+                e0 = lane < nb ? trow[jb0 + lane] : 0;
+                e1 = lane + 32 < nb ? trow[jb0 + lane + 32] : 0;
+            }
             if ((lane < nb && (e0 < 0 || e0 >= p.num_blocks)) ||
                 (lane + 32 < nb && (e1 < 0 || e1 >= p.num_blocks))) {
                 set_status(p.status, PKV_DEV_BAD_BLOCK_ID);
@@ -416,7 +441,7 @@ __global__ void __launch_bounds__(SimtCfg<QT, KT, HD, HPI>::THREADS, 2)
                 }
                 if (++stage == Cfg::NSTAGE) { stage = 0; phase ^= 1u; }
             }
-            w = __shfl_sync(0xffffffffu, wn, 0);
+            w = p.self_plan ? wn : __shfl_sync(0xffffffffu, wn, 0);
         }
         if (ok) {
             if (mbar_wait(&empty[stage], phase ^ 1u)) {

@@ -37,11 +37,28 @@ cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
         occ.ctas[dev] = (per_sm > 0 ? per_sm : 1) * sms;
     }
+    // the decode kernel starts launching while its predecessor runs and waits for it
+    // on the device (programmatic dependent launch)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)occ.ctas[dev], 1, 1);
+    cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (p.self_plan) {
+        // every context within one chunk: the decode kernel plans for itself
+        const long long units = (long long)p.num_seqs * p.num_kv_heads * p.nsub;
+        cfg.gridDim.x = (unsigned)(units < occ.ctas[dev] ? units : occ.ctas[dev]);
+        return cudaLaunchKernelEx(&cfg, kernel, p);
+    }
     plan_kernel<QT><<<1, 1024, 0, stream>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    kernel<<<occ.ctas[dev], Cfg::THREADS, smem, stream>>>(p);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 // Tensor-core variant: 16-bit q, 16-bit or FP8 K/V, 8 query heads per item.
@@ -95,8 +112,13 @@ cudaError_t launch_decode_mma_nt(const DecodeParams& p, cudaStream_t stream) {
         pc.numAttrs = 1;
         err = cudaLaunchKernelEx(&pc, plan_split_kernel<QT>, ps);
     } else {
-        plan_split_kernel<QT><<<1, 1024, 0, stream>>>(ps);
-        err = cudaGetLastError();
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(1, 1, 1);
+        pc.blockDim = dim3(1024, 1, 1);
+        pc.stream = stream;
+        pc.attrs = pdl;
+        pc.numAttrs = 1;
+        err = cudaLaunchKernelEx(&pc, plan_split_kernel<QT>, ps);
     }
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};

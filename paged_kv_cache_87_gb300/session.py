@@ -109,6 +109,24 @@ class DeviceState:
         self.append_step(stream)
         return self.decode(stream)
 
+    def prepare(self, stream=None) -> tuple:
+        """The step's calls with their arguments marshalled once, for `stream`:
+        (copy-on-write + append calls, decode call).  Re-prepare after the inputs
+        move (pack_step_inputs)."""
+        w = self.w
+        pre = []
+        if self.step_pairs.numel():
+            pre.append(binding.prepare_copy_blocks(self.k_cache, self.v_cache, self.step_pairs,
+                                                   stream=stream))
+        pre.append(binding.prepare_reshape_and_cache(self.new_key, self.new_value, self.k_cache,
+                                                     self.v_cache, self.new_slots,
+                                                     kv_scale=w.kv_scale, stream=stream))
+        dec = binding.prepare_paged_decode_attention(
+            self.query, self.k_cache, self.v_cache, self.block_tables, self.context_lens,
+            w.max_context_len, w.scale, kv_scale=w.kv_scale, workspace=self.workspace,
+            out=self.out, stream=stream, prefix=self.prefix)
+        return tuple(pre), dec
+
     def out_f64(self) -> np.ndarray:
         return self.out.detach().to(torch.float64).cpu().numpy()
 

@@ -215,3 +215,22 @@ def test_context_above_max_context_len_is_clamped_and_flagged():
     kc, vc = oracle_caches(w)
     ref = oracle_decode(w, kc, vc, context_lens=np.minimum(w.context_lens, 64))
     _check(w, st.out_f64(), ref)
+
+
+@pytest.mark.parametrize("d,B,Hq,Hkv", [(64, 16, 8, 8), (128, 8, 8, 2), (64, 32, 12, 4),
+                                        (128, 16, 16, 2)])
+@pytest.mark.parametrize("qdt,kvdt", [("f32", "f32"), ("f32", "e4m3"), ("bf16", "e4m3")])
+def test_single_launch_small_contexts(d, B, Hq, Hkv, qdt, kvdt):
+    """Every context within one 512-token chunk: the CUDA-core path launches only the
+    decode kernel, which takes its work items from the sequence index; empty
+    sequences get zeros."""
+    rng = np.random.default_rng(zlib.crc32(repr(("small", d, B, Hq, Hkv, qdt, kvdt)).encode()))
+    ctx = np.array([0, 1, B - 1, B, B + 1, 100, 511, 512, 0, 300])
+    w = inputs.make_independent("small", rng, ctx, num_q_heads=Hq, num_kv_heads=Hkv,
+                                head_dim=d, block_size=B, q_dtype=qdt, kv_dtype=kvdt,
+                                scale=1.0 / math.sqrt(d),
+                                kv_scale=2.0 ** -5 if kvdt == "e4m3" else 1.0)
+    assert w.max_context_len <= 512
+    st, _ = _full_parity(w)
+    out = st.out_f64()
+    assert (out[0] == 0).all() and (out[8] == 0).all()
