@@ -234,3 +234,24 @@ def test_single_launch_small_contexts(d, B, Hq, Hkv, qdt, kvdt):
     st, _ = _full_parity(w)
     out = st.out_f64()
     assert (out[0] == 0).all() and (out[8] == 0).all()
+
+
+@pytest.mark.parametrize("qdt,kvdt,B", [("bf16", "bf16", 16), ("f16", "e4m3", 8)])
+def test_many_short_units_over_every_cta(qdt, kvdt, B):
+    """320 sequences of one or two chunks (about 10 tiles per CTA of the balanced split):
+    many units straddle two CTAs' ranges.  Elementwise parity, then three more decodes
+    must be bit-identical (every segment's partial state has a fixed slot and the
+    merge runs in segment order)."""
+    rng = np.random.default_rng(zlib.crc32(repr(("tail", qdt, kvdt, B)).encode()))
+    ctx = rng.integers(1, 1100, size=320)
+    ctx[:7] = [1, 63, 64, 65, 512, 513, 1099]
+    w = inputs.make_independent("many short", rng, ctx, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, block_size=B, q_dtype=qdt, kv_dtype=kvdt,
+                                scale=1.0 / math.sqrt(128),
+                                kv_scale=2.0 ** -5 if kvdt == "e4m3" else 1.0)
+    st, _ = _full_parity(w)
+    first = st.out.clone()
+    for _ in range(3):
+        st.decode()
+        torch.cuda.synchronize()
+        assert torch.equal(first.view(torch.int16), st.out.view(torch.int16))

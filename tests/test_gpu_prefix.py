@@ -150,3 +150,20 @@ def test_member_rows_that_diverge_inside_the_prefix(pad):
         assert t[seq, j] != donor and j * 16 + 16 <= w.context_lens[seq] - 64
         t[seq, j] = donor
     _check(dataclasses.replace(w, block_tables=t))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_many_groups_split_over_every_cta(kv):
+    """48 groups of 4 samples: shared and private units cut across many CTAs' ranges,
+    merged per member; a repeated decode is bit-identical."""
+    rng = np.random.default_rng(41 if kv == "bf16" else 42)
+    w = inputs.make_shared_prefix("many groups", rng, num_groups=48, samples=4, prefix_lo=600,
+                                  prefix_hi=2500, tail_lo=1, tail_hi=200, num_q_heads=32,
+                                  num_kv_heads=8, head_dim=128, block_size=16, q_dtype="bf16",
+                                  kv_dtype=kv, kv_scale=2.0 ** -5 if kv == "e4m3" else 1.0,
+                                  scale=1 / math.sqrt(128))
+    st = _check(w)
+    first = st.out.clone()
+    st.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), st.out.view(torch.int16))
