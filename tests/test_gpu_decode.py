@@ -79,7 +79,7 @@ def test_config_full_size_sampled(cid):
 SWEEP = []
 for d in (64, 128):
     for B in (8, 16, 32):
-        for (Hq, Hkv) in ((4, 4), (6, 2), (8, 2), (10, 2), (16, 2)):
+        for (Hq, Hkv) in ((4, 4), (4, 2), (6, 2), (8, 2), (10, 2), (16, 2)):
             SWEEP.append((d, B, Hq, Hkv))
 
 
@@ -92,7 +92,7 @@ DTYPE_PAIRS = [("f32", "f32"), ("f32", "e4m3"), ("f16", "f16"), ("f16", "e4m3"),
 @pytest.mark.parametrize("qdt,kvdt", DTYPE_PAIRS)
 def test_sweep_shapes_and_types(d, B, Hq, Hkv, qdt, kvdt):
     """Every shipped decode variant (q type, KV type, head_dim, block size, and
-    heads per kv head 1, 3, 4, 5 and 8) against the oracle, elementwise."""
+    heads per kv head 1, 2, 3, 4, 5 and 8) against the oracle, elementwise."""
     rng = np.random.default_rng(zlib.crc32(repr((d, B, Hq, Hkv, qdt, kvdt)).encode()))
     ctx = np.array([1, B - 1, B, B + 1, 511, 512, 513, 1100, 0, 3000])
     w = inputs.make_independent("sweep", rng, ctx, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d,
@@ -255,3 +255,34 @@ def test_many_short_units_over_every_cta(qdt, kvdt, B):
         st.decode()
         torch.cuda.synchronize()
         assert torch.equal(first.view(torch.int16), st.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("cid,kw,prefix", [(1, dict(num_seqs=8), False),
+                                           (2, dict(num_seqs=32), False),
+                                           (4, dict(num_seqs=16, ctx_cap=1500), True)])
+def test_step_replays_in_a_cuda_graph(cid, kw, prefix):
+    """The hot-path step (copy-on-write, cache write, decode: planner, decode kernel and
+    for the prefix-aware entry the shared-prefix detection and the merge) captured in a
+    CUDA graph after one eager step: every replay reproduces the eager output bit for
+    bit (the step is idempotent)."""
+    w = inputs.make_config(cid, **kw)
+    st = gpu_state(w, prefix=prefix)
+    eager = st.out.clone()
+    stream = torch.cuda.Stream()
+    pre, dec = st.prepare(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c in pre:
+            c()
+        dec()
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for c in pre:
+                c()
+            dec()
+        for _ in range(2):
+            st.out.zero_()
+            graph.replay()
+            stream.synchronize()
+            assert torch.equal(eager.view(torch.int16), st.out.view(torch.int16))
+    assert binding.pkv_get_device_status() == 0
