@@ -23,10 +23,13 @@
 //   warps 0-3  tile A, one thread per row: the softmax of each S tile, the
 //              rescale of O, the epilogue;
 //   warps 4-7  the same for tile B;
-//   warp 8     takes the items; TMA producer: the item's Q rows, then K_0, V_0,
-//              K_1, V_1, ... into a 5-stage ring, one 4-D box per (block, kv
-//              head) row of the pool;
-//   warp 9     TMEM allocation; one lane issues the MMAs; warps 10-11 idle.
+//   warp 8     takes the items and decodes each into the CTA's item ring (a
+//              sequence, a kv head, row ranges, tile counts); TMA producer: the
+//              item's Q rows, then K_0, V_0, K_1, V_1, ... into a 5-stage ring,
+//              one 4-D box per (block, kv head) row of the pool;
+//   warp 9     TMEM allocation; one lane issues the MMAs;
+//   warp 10    prefetches each published item's Q rows into L2 (the Q buffer
+//              frees only with the previous item's last S MMAs); warp 11 idle.
 // Per 128-token tile j and row tile X:  S_X = Q_X K_j^T (M 128, N 128, K 128;
 // Q from shared memory, S in TMEM), then O_X += P_X V_j (P in TMEM, written
 // over the first 64 columns of S_X as 16-bit pairs; V an MN-major operand).
@@ -63,7 +66,8 @@ constexpr int kStages = 5;                            // K/V ring: K_0, V_0, K_1
 constexpr int kOffQ = 0;                              // Q_A, Q_B: [half][128 rows][128 B]
 constexpr int kOffRing = kOffQ + 2 * kTileBytes;
 constexpr int kOffBars = kOffRing + kStages * kTileBytes;
-constexpr int kSmem = kOffBars + 256 + 1024;          // barriers, TMEM slot, flag, item ring; alignment
+constexpr int kOffItems = kOffBars + 256;             // the two-slot ring of decoded items
+constexpr int kSmem = kOffItems + 2 * 64 + 1024;      // barriers, TMEM slot, flag; item ring; alignment
 constexpr int kThreads = 384;                         // 8 row warps; producer, MMA, 2 idle
 // registers per thread after the split: the row warpgroups take what the third
 // warpgroup gives back (216 x 256 + 72 x 128 = 168 x 384, the launch's budget)
@@ -81,9 +85,9 @@ static_assert(kMqRows == 2 * kTile, "a CTA holds two row tiles");
 static_assert(kRowRegs * 256 + kAuxRegs * 128 <= (65536 / kThreads) / 8 * 8 * kThreads,
               "the register split fits the launch's registers");
 static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-constexpr int kItemReaders = 9;                       // warps reading each item index
+constexpr int kItemReaders = 10;                      // warps reading each item
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 1 + 1 + 2 + 2 + 2 + 1;
-static_assert(kNumBars * 8 + 16 <= 256, "barriers, TMEM slot, flag and item ring fit their region");
+static_assert(kNumBars * 8 + 8 <= 256, "barriers, TMEM slot and flag fit their region");
 
 template <typename QT>
 __device__ __forceinline__ uint32_t pack2(float a, float b, float& ra, float& rb) {
@@ -109,6 +113,14 @@ __device__ __forceinline__ uint32_t pack2_bits(float a, float b) {
         const __half2 h = __floats2half2_rn(a, b);
         return *reinterpret_cast<const uint32_t*>(&h);
     }
+}
+
+// One 32-byte store (sm_100 family); dst 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                 "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 // Packed fp32 pairs (sm_100 family): one instruction for two lanes of work.
@@ -224,14 +236,29 @@ struct MqItem {
     int kv_end;                    // tokens the item stages
 };
 
-// Item `idx` in launch order: the last sequence (in launch order) whose first item
-// is <= idx, then its row pair (later, longer pairs first) and its kv head.
+// An entry of the CTA's item ring: the item decoded by the producer warp, so that the
+// MMA and row warps start the next item without a chain of global loads of their own.
+struct __align__(16) MqSlot {
+    MqItem it;
+    int idx;                       // the item's index in launch order; -1: no items left
+    int pad;
+};
+static_assert(sizeof(MqSlot) == 64, "two item slots fill 128 bytes");
+
+// Item `idx` in launch order (called by a whole warp; every lane gets the item): the
+// last sequence (in launch order) whose first item is <= idx, found by a 32-way search
+// (one load per lane and round: one round up to 32 sequences, two up to 1024), then its
+// row pair (later, longer pairs first) and its kv head.
 __device__ __forceinline__ MqItem mq_item(const MqParams& p, int idx) {
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(&p.item_prefix[mid]) <= idx) lo = mid;
-        else hi = mid - 1;
+    const int lane = threadIdx.x & 31;
+    int lo = 0, len = p.num_seqs;                 // item_prefix[lo] <= idx; answer in [lo, lo + len)
+    while (len > 1) {
+        const int step = (len + 31) >> 5;
+        const int pos = lo + lane * step;
+        const bool le = pos < lo + len && __ldg(&p.item_prefix[pos]) <= idx;
+        const int last = 31 - __clz(__ballot_sync(0xffffffffu, le));   // lane 0 always holds
+        lo += last * step;
+        len = min(step, len - last * step);
     }
     MqItem it;
     it.s = __ldg(&p.seq_order[lo]);
@@ -255,15 +282,16 @@ __device__ __forceinline__ MqItem mq_item(const MqParams& p, int idx) {
     return it;
 }
 
-// The CTA's k-th item index (-1: none left), published by the producer warp in a
+// The CTA's k-th item (index -1: none left), published by the producer warp in a
 // two-slot ring; each reading warp releases the slot with one arrival (lane 0).
-__device__ __forceinline__ int mq_take_item(const volatile int* items_s, uint64_t* item_full,
-                                            uint64_t* item_empty, int k, volatile int* abort_flag,
-                                            unsigned* status) {
+__device__ __forceinline__ int mq_take_item(const MqSlot* items_s, uint64_t* item_full,
+                                            uint64_t* item_empty, int k, MqItem& it,
+                                            volatile int* abort_flag, unsigned* status) {
     const int slot = k & 1;
     int idx = -1;
     if (mbar_wait(&item_full[slot], (k >> 1) & 1)) {
-        idx = items_s[slot];
+        idx = items_s[slot].idx;
+        if (idx >= 0) it = items_s[slot].it;
     } else {
         set_status(status, PKV_DEV_WAIT_TIMEOUT);
         *abort_flag = 1;
@@ -278,7 +306,7 @@ __device__ __forceinline__ void mq_producer(const MqParams& p, const CUtensorMap
                                             const CUtensorMap* tmV, const CUtensorMap* tmQ,
                                             uint8_t* smem, uint64_t* full, uint64_t* empty,
                                             uint64_t* q_full, uint64_t* q_free,
-                                            volatile int* items_s, uint64_t* item_full,
+                                            MqSlot* items_s, uint64_t* item_full,
                                             uint64_t* item_empty, volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -295,9 +323,9 @@ __device__ __forceinline__ void mq_producer(const MqParams& p, const CUtensorMap
         // the next item, taken from the launch-wide counter once this warp has issued
         // every load of the previous one: CTAs take items in launch order, longest
         // first, about two tile pairs before they finish their current item
+        const int slot = k & 1;
         int idx = -1;
         if (lane == 0) {
-            const int slot = k & 1;
             if (!mbar_wait(&item_empty[slot], ((k >> 1) & 1) ^ 1u)) {
                 set_status(p.status, PKV_DEV_WAIT_TIMEOUT);
                 *abort_flag = 1;
@@ -305,12 +333,16 @@ __device__ __forceinline__ void mq_producer(const MqParams& p, const CUtensorMap
                 idx = atomicAdd(p.work_next, 1);
                 if (idx >= total) idx = -1;
             }
-            items_s[slot] = idx;
-            mbar_arrive(&item_full[slot]);
         }
         idx = __shfl_sync(0xffffffffu, idx, 0);
+        MqItem it{};
+        if (idx >= 0) it = mq_item(p, idx);
+        if (lane == 0) {
+            items_s[slot].it = it;
+            items_s[slot].idx = idx;
+            mbar_arrive(&item_full[slot]);
+        }
         if (idx < 0) break;
-        const MqItem it = mq_item(p, idx);
         const int32_t* trow = p.block_tables + (int64_t)it.s * p.max_blocks;
         const int nb_all = (it.kv_end + B - 1) / B;   // table entries this item reads
         // block-table window: lane l holds entry wb + l (cur) and wb + 32 + l (nxt); the
@@ -384,7 +416,7 @@ __device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_
                                        uint64_t* full, uint64_t* empty, uint64_t* s_full,
                                        uint64_t* p_full, uint64_t* q_full, uint64_t* q_free,
                                        uint64_t* drain, uint64_t* o_free, uint64_t* fin,
-                                       const volatile int* items_s, uint64_t* item_full,
+                                       const MqSlot* items_s, uint64_t* item_full,
                                        uint64_t* item_empty, volatile int* abort_flag) {
     constexpr bool kBF16 = std::is_same<QT, BF16>::value;
     constexpr uint32_t idqk = tc5::idesc_f16(kBF16, kTile, kTile, false, false);
@@ -432,9 +464,9 @@ __device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_
     bool ok = true;
     uint32_t rbase = 0, np_a = 0, np_b = 0;              // ring entries; P tiles consumed
     for (int k = 0; ok; ++k) {
-        const int idx = mq_take_item(items_s, item_full, item_empty, k, abort_flag, p.status);
+        MqItem it{};
+        const int idx = mq_take_item(items_s, item_full, item_empty, k, it, abort_flag, p.status);
         if (idx < 0 || *abort_flag) break;
-        const MqItem it = mq_item(p, idx);
         if (!wait_bar(q_full, k & 1) || !wait_entry(rbase)) { ok = false; break; }
         issue_s(0, (int)(rbase % kStages));
         if (it.T_b > 0) issue_s(1, (int)(rbase % kStages));
@@ -479,7 +511,9 @@ __device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_
 }
 
 // TREE: draft-tree verification (the ancestor masks of p.tree) instead of causal attention.
-template <typename QT, bool TREE>
+// OUT32: the output is 32-byte aligned, and each row's 256 bytes go out as 32-byte stores
+// (one whole sector each) instead of 16-byte ones.
+template <typename QT, bool TREE, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     MqParams p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const __grid_constant__ CUtensorMap tmQ) {
@@ -500,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
     uint64_t* fin = item_empty + 2;              // every MMA of the CTA completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* items_s = abort_flag + 1;      // [2] the item ring
+    MqSlot* items_s = reinterpret_cast<MqSlot*>(smem + kOffItems);   // [2] the item ring
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -539,6 +573,18 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 mq_mma<QT>(p, smem, tmem, full, empty, s_full, p_full, q_full, q_free, drain, o_free,
                            fin, items_s, item_full, item_empty, abort_flag);
             __syncwarp();
+        } else if (warp == 10) {
+            // each item's Q rows into L2 as soon as the item is published, about two tile
+            // pairs before the Q buffer frees (with the previous item's last S MMAs)
+            for (int k = 0;; ++k) {
+                MqItem it{};
+                const int idx = mq_take_item(items_s, item_full, item_empty, k, it, abort_flag,
+                                             p.status);
+                if (idx < 0) break;
+                if (lane < 4 && (lane < 2 || it.qn_b > 0))
+                    tc5::tma_prefetch_3d(&tmQ, 64 * (lane & 1), it.kvh * p.group,
+                                         it.q_begin + it.q0 + (lane >> 1) * (kTile / p.group));
+            }
         }
         // the TMEM is released once every thread is past its last use
         tc5::fence_before_sync();
@@ -560,9 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
         const int G = p.group, qpt = kTile / G;
         bool ok = true;
         uint32_t rbase = 0, ns = 0;                       // ring entries; S_X tiles seen
-        int idx = mq_take_item(items_s, item_full, item_empty, 0, abort_flag, p.status);
         MqItem it{};
-        if (idx >= 0) it = mq_item(p, idx);
+        int idx = mq_take_item(items_s, item_full, item_empty, 0, it, abort_flag, p.status);
         for (int k = 0; idx >= 0 && ok; ++k) {
             const int Tx = X ? it.T_b : it.T_a;
             const int qi = it.q0 + X * qpt + r / G;
@@ -685,9 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
             rbase += 2u * (uint32_t)it.T;
             // the next item (its Q arrives by TMA: the MMAs of the next item may start
             // while this one's epilogue runs)
-            idx = mq_take_item(items_s, item_full, item_empty, k + 1, abort_flag, p.status);
             MqItem nx{};
-            if (idx >= 0) nx = mq_item(p, idx);
+            idx = mq_take_item(items_s, item_full, item_empty, k + 1, nx, abort_flag, p.status);
             // epilogue: every MMA of this item has completed (every thread waits, so the
             // drain barrier's phases stay in step with the items)
             ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(drain, k & 1));
@@ -703,18 +747,23 @@ __global__ void __launch_bounds__(kThreads, 1) mq_attention_kernel(
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t w[16];
+                    // packed in place: pair e of the chunk overwrites word e (<= 2e)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float ra, rb;
-                        w[e] = pack2<QT>(__uint_as_float(ov[c4][2 * e]) * inv,
-                                         __uint_as_float(ov[c4][2 * e + 1]) * inv, ra, rb);
+                        ov[c4][e] = pack2<QT>(__uint_as_float(ov[c4][2 * e]) * inv,
+                                              __uint_as_float(ov[c4][2 * e + 1]) * inv, ra, rb);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qrow +
-                                                          c4 * 32);
+                    uint16_t* dst = static_cast<uint16_t*>(p.out) + qrow + c4 * 32;
+                    if constexpr (OUT32) {
+                        st_global_v8(dst, ov[c4]);
+                        st_global_v8(dst + 16, ov[c4] + 8);
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            reinterpret_cast<uint4*>(dst)[e] = make_uint4(
+                                ov[c4][4 * e], ov[c4][4 * e + 1], ov[c4][4 * e + 2], ov[c4][4 * e + 3]);
+                    }
                 }
             }
             it = nx;
@@ -735,14 +784,15 @@ cudaError_t launch_typed(const MqParams& p, int64_t max_items, int num_ctas, cud
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    auto kernel = p.tree ? mq_attention_kernel<QT, true> : mq_attention_kernel<QT, false>;
+    const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
+    auto kernel = p.tree ? (out32 ? mq_attention_kernel<QT, true, true> : mq_attention_kernel<QT, true, false>)
+                         : (out32 ? mq_attention_kernel<QT, false, true> : mq_attention_kernel<QT, false, false>);
     if (!attr_set[dev]) {
-        err = cudaFuncSetAttribute(mq_attention_kernel<QT, false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(mq_attention_kernel<QT, true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (err != cudaSuccess) return err;
+        for (auto f : {mq_attention_kernel<QT, false, false>, mq_attention_kernel<QT, false, true>,
+                       mq_attention_kernel<QT, true, false>, mq_attention_kernel<QT, true, true>}) {
+            err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+            if (err != cudaSuccess) return err;
+        }
         attr_set[dev] = true;
     }
     CUtensorMap tk, tv;

@@ -227,6 +227,39 @@ def test_launch_order_leaves_every_sequence_bit_identical():
     assert torch.equal(a[torch.from_numpy(rows).to(a.device)], b)
 
 
+def _offset_out(like: torch.Tensor) -> torch.Tensor:
+    """An output tensor shaped like `like` whose data starts 16 bytes past a 32-byte
+    boundary (the kernel then writes 16-byte pieces instead of 32-byte ones)."""
+    buf = torch.empty(like.numel() + 64, dtype=like.dtype, device=like.device)
+    base = buf.data_ptr()
+    skip = ((-base) % 32 + 16) // like.element_size()
+    out = buf[skip:skip + like.numel()].view(like.shape)
+    assert out.data_ptr() % 32 == 16
+    return out
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_output_16_byte_aligned_only_is_bit_identical(tree):
+    """The 32-byte-store and 16-byte-store epilogues write the same bits."""
+    rng = np.random.default_rng(31)
+    prior, n = [300, 0, 1000, 77], [64, 33 if tree else 200, 40, 9]
+    if tree:
+        w = inputs.make_tree_verify("tree-align", rng, prior, n, num_q_heads=8, num_kv_heads=2,
+                                    head_dim=128, block_size=16, dtype="bf16")
+        st = _check_tree(w)
+    else:
+        w = inputs.make_multi_query("align", rng, prior, n, num_q_heads=8, num_kv_heads=2,
+                                    head_dim=128, block_size=16, dtype="bf16")
+        st = _check(w)
+    assert st.out.data_ptr() % 32 == 0
+    out16 = _offset_out(st.out)
+    out16.fill_(float("nan"))
+    st.attend(out=out16)
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() == 0
+    assert torch.equal(out16, st.out)
+
+
 # ------------------------------------------------------------ draft trees --
 
 def _oracle_tree(w, sel=None):
