@@ -481,15 +481,22 @@ __device__ __forceinline__ void mq_mma(const MqParams& p, uint8_t* smem, uint32_
             const uint32_t gv = rbase + 2u * j + 1u, gk = gv + 1u;
             const int vs = (int)(gv % kStages), ks = (int)(gk % kStages);
             const bool next = j + 1 < it.T;
-            if (!wait_entry(gv)) { ok = false; break; }
-            if (j < it.T_a) {
-                if (!wait_bar(&p_full[0], np_a++ & 1)) { ok = false; break; }
-                issue_pv(0, vs, j > 0);
+            // V_j and K_j+1 have normally landed long before; the fence that orders the
+            // MMAs after these waits comes once per burst, after the wait for P
+            if (!mbar_wait(&full[vs], (gv / kStages) & 1) ||
+                (next && !mbar_wait(&full[ks], (gk / kStages) & 1))) {
+                ok = false;
+                break;
             }
-            if (next && !wait_entry(gk)) { ok = false; break; }
-            if (j + 1 < it.T_a) issue_s(0, ks);
+            if (j < it.T_a) {
+                if (!mbar_wait(&p_full[0], np_a++ & 1)) { ok = false; break; }
+                tc5::fence_after_sync();
+                issue_pv(0, vs, j > 0);
+                if (j + 1 < it.T_a) issue_s(0, ks);
+            }
             if (j < it.T_b) {
-                if (!wait_bar(&p_full[1], np_b++ & 1)) { ok = false; break; }
+                if (!mbar_wait(&p_full[1], np_b++ & 1)) { ok = false; break; }
+                tc5::fence_after_sync();
                 issue_pv(1, vs, j > 0);
             }
             tc5::commit(&empty[vs]);
