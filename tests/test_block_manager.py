@@ -192,3 +192,66 @@ def test_prepare_step_needs_only_the_copies_it_makes():
     with pytest.raises(binding.PagedKVError):
         m3.prepare_step([0, 1, 2], 4)      # two copies, one free block: refused
     assert [m3.refcount(b) for b in range(4)] == before and m3.num_free == 1
+
+
+def _beam_invariants(m, live, NB):
+    """Every block's reference count is the number of live beams whose table holds it;
+    the free count is what no live beam holds."""
+    held = {}
+    for s in live:
+        table, _ = m.sequence(s)
+        for b in table:
+            held[b] = held.get(b, 0) + 1
+    for b in range(NB):
+        assert m.refcount(b) == held.get(b, 0), b
+    assert m.num_free == NB - len(held)
+    return held
+
+
+def test_beam_search_prunes_and_forks_by_reference_counts():
+    """Beam search ("...Mathematical Foundations" §5 Beam Search): each step every live
+    beam appends a token, then K survivors are forked from chosen parents and the old
+    beams dropped. Only block tables and reference counts change: survivors share the
+    parents' blocks, discarded beams give theirs back, and copy-on-write copies happen
+    only where a shared block is written."""
+    B, NB, K, prompt = 4, 128, 4, 10
+    rng = np.random.default_rng(7)
+    m = binding.BlockManager(NB, B)
+    m.add_sequence(0, prompt)
+    live, next_id = [0], 1
+    for c in range(1, K):                     # the first K beams fork the prompt
+        m.fork(0, c)
+        live.append(c)
+    next_id = K
+    tokens = {s: prompt for s in live}
+    copies = 0
+    for step in range(12):
+        slots, pairs, tables, ctx = m.prepare_step(live, 16)
+        copies += len(pairs)
+        for i, s in enumerate(live):
+            tokens[s] += 1
+            assert ctx[i] == tokens[s]
+            assert slots[i] == tables[i][(tokens[s] - 1) // B] * B + (tokens[s] - 1) % B
+        # every copy's destination is a fresh block held by exactly one beam
+        for _, dst in pairs:
+            assert m.refcount(int(dst)) == 1
+        _beam_invariants(m, live, NB)
+        # selection: K new beams, each a fork of a parent drawn from the live ones
+        # (some parents several times, some not at all), then the old beams go
+        parents = rng.choice(live, size=K, replace=True)
+        new = []
+        for par in parents:
+            m.fork(int(par), next_id)
+            tokens[next_id] = tokens[int(par)]
+            new.append(next_id)
+            next_id += 1
+        for s in live:
+            m.free_sequence(s)
+        live = new
+        held = _beam_invariants(m, live, NB)
+        # survivors share history: fewer blocks than K private copies would take
+        assert len(held) < K * -(-max(tokens[s] for s in live) // B)
+    assert copies > 0
+    for s in live:
+        m.free_sequence(s)
+    assert m.num_free == NB and all(m.refcount(b) == 0 for b in range(NB))
