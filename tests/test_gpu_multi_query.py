@@ -80,6 +80,47 @@ def test_prompts_without_prior_context_ragged_tiles():
     _check(w)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (32, 1)])
+def test_prompts_of_many_lengths(Hq, Hkv):
+    """Prompts without prior context: ties, a prompt of zero tokens, prompts shorter than
+    one row pair and prompts of many pairs, against the oracle."""
+    rng = np.random.default_rng(23 + Hq)
+    n = [700, 700, 0, 1, 255, 1300, 64, 513, 256, 900]
+    w = inputs.make_multi_query("prompts", rng, [0] * len(n), n, num_q_heads=Hq,
+                                num_kv_heads=Hkv, head_dim=128, block_size=16, dtype="bf16")
+    _check(w)
+
+
+def test_prompt_order_leaves_every_prompt_bit_identical():
+    """Each prompt's items are computed the same way wherever the planner puts them:
+    permuting the prompts permutes the output rows, bit for bit, and a prompt run alone
+    gives the same bits."""
+    rng = np.random.default_rng(24)
+    n = [300, 1025, 17, 600, 600, 90]
+    w = inputs.make_multi_query("prompts", rng, [0] * len(n), n, num_q_heads=8, num_kv_heads=2,
+                                head_dim=128, block_size=16, dtype="f16")
+    a = _gpu(w).out.clone()
+    perm = np.array([4, 1, 5, 0, 3, 2])
+    qs = w.query_start
+    rows = np.concatenate([np.arange(qs[s], qs[s + 1]) for s in perm])
+    nn = np.diff(qs)[perm]
+    w2 = inputs.MultiQueryWorkload(**{**w.__dict__, "query": w.query[rows],
+                                      "block_tables": w.block_tables[perm],
+                                      "context_lens": w.context_lens[perm],
+                                      "query_start": np.concatenate([[0], np.cumsum(nn)]).astype(np.int32),
+                                      "seq_tokens": [w.seq_tokens[s] for s in perm]})
+    b = _gpu(w2).out
+    assert binding.pkv_get_device_status() == 0
+    assert torch.equal(a[torch.from_numpy(rows).to(a.device)], b)
+    one = inputs.MultiQueryWorkload(**{**w.__dict__, "num_seqs": 1, "query": w.query[qs[1]:qs[2]],
+                                       "block_tables": w.block_tables[1:2],
+                                       "context_lens": w.context_lens[1:2],
+                                       "query_start": np.array([0, n[1]], np.int32),
+                                       "seq_tokens": [w.seq_tokens[1]]})
+    c = _gpu(one).out
+    assert torch.equal(a[int(qs[1]):int(qs[2])], c)
+
+
 def test_long_prior_context_many_kv_tiles():
     rng = np.random.default_rng(22)
     w = inputs.make_multi_query("long", rng, [3000, 1700], [200, 70], num_q_heads=8,
