@@ -80,6 +80,23 @@ def test_prompts_without_prior_context_ragged_tiles():
     _check(w)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(64, 1), (128, 1), (128, 2)])
+@pytest.mark.parametrize("tree", [False, True])
+def test_widest_head_groups(Hq, Hkv, tree):
+    """64 and 128 query heads per kv head: a row tile holds two or one query tokens of
+    every head of the group (the Q box is 64 elements x G heads x 128 / G tokens)."""
+    rng = np.random.default_rng(25 + Hq + Hkv)
+    prior, n = [0, 130, 1000, 5], [9, 40, 3, 64]
+    if tree:
+        w = inputs.make_tree_verify("wide-tree", rng, prior, n, num_q_heads=Hq, num_kv_heads=Hkv,
+                                    head_dim=128, block_size=16, dtype="bf16")
+        _check_tree(w)
+    else:
+        w = inputs.make_multi_query("wide", rng, prior, n, num_q_heads=Hq, num_kv_heads=Hkv,
+                                    head_dim=128, block_size=16, dtype="bf16")
+        _check(w)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4), (32, 1)])
 def test_prompts_of_many_lengths(Hq, Hkv):
     """Prompts without prior context: ties, a prompt of zero tokens, prompts shorter than
