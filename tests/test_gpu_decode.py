@@ -286,3 +286,25 @@ def test_step_replays_in_a_cuda_graph(cid, kw, prefix):
             stream.synchronize()
             assert torch.equal(eager.view(torch.int16), st.out.view(torch.int16))
     assert binding.pkv_get_device_status() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 2), (64, 2), (128, 1)])
+@pytest.mark.parametrize("qdt,kvdt", [("bf16", "bf16"), ("f16", "e4m3"), ("f32", "f32")])
+@pytest.mark.parametrize("prefix", [False, True])
+def test_wide_head_groups(Hq, Hkv, qdt, kvdt, prefix):
+    """16 to 128 query heads per kv head: the tensor-core kernel serves a kv head's group
+    in subgroups of 8 heads (each a work unit of its own), the CUDA-core kernel in items
+    of up to 4; contexts over several chunks are split and merged. The prefix-aware
+    entry point cannot group sequences here (more than 8 heads per kv head), so it runs
+    the same units through its own planner and merge."""
+    rng = np.random.default_rng(zlib.crc32(repr(("wide", Hq, Hkv, qdt, kvdt, prefix)).encode()))
+    ctx = np.array([1, 100, 700, 1500, 0, 33])
+    w = inputs.make_independent("wide", rng, ctx, num_q_heads=Hq, num_kv_heads=Hkv,
+                                head_dim=128, block_size=16, q_dtype=qdt, kv_dtype=kvdt,
+                                scale=1.0 / math.sqrt(128),
+                                kv_scale=2.0 ** -5 if kvdt == "e4m3" else 1.0)
+    st = gpu_state(w, prefix=prefix)
+    kc, vc = oracle_caches(w)
+    ref = oracle_decode(w, kc, vc, nthreads=8)
+    _check(w, st.out_f64(), ref)
+    assert binding.pkv_get_device_status() == 0
