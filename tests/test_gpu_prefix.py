@@ -167,3 +167,29 @@ def test_many_groups_split_over_every_cta(kv):
     st.decode()
     torch.cuda.synchronize()
     assert torch.equal(first.view(torch.int16), st.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("prefix", [True, False])
+def test_more_records_than_the_planner_keeps_in_shared_memory(prefix):
+    """1,500 groups of 3 samples: 1,500 group records and 4,500 private ones, beyond the
+    4,096 record offsets the planner keeps in shared memory, so the workers find their
+    first record in the global copy."""
+    rng = np.random.default_rng(23)
+    w = inputs.make_shared_prefix("records", rng, num_groups=1500, samples=3, prefix_lo=32,
+                                  prefix_hi=96, tail_lo=1, tail_hi=30, num_q_heads=8,
+                                  num_kv_heads=2, head_dim=128, block_size=16, q_dtype="bf16",
+                                  kv_dtype="bf16", kv_scale=1.0, scale=1 / math.sqrt(128))
+    assert w.num_seqs == 4500
+    _check(w, prefix=prefix)
+
+
+def test_plain_batch_beyond_the_planner_record_cache():
+    """5,000 independent sequences: one record each, beyond the planner's 4,096 cached
+    record offsets."""
+    rng = np.random.default_rng(24)
+    ctx = rng.integers(0, 200, size=5000)
+    w = inputs.make_independent("records", rng, ctx, num_q_heads=8, num_kv_heads=2,
+                                head_dim=128, block_size=16, q_dtype="bf16", kv_dtype="bf16",
+                                scale=1 / math.sqrt(128))
+    st = _check(w, prefix=False)
+    assert (st.out_f64()[ctx == 0] == 0).all()
