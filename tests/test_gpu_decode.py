@@ -205,6 +205,24 @@ def test_bad_block_id_is_flagged_not_faulted():
     assert binding.pkv_get_device_status() & binding.DEV_BAD_BLOCK_ID
 
 
+@pytest.mark.parametrize("qdt,kvdt,prefix", [("bf16", "bf16", False), ("bf16", "bf16", True),
+                                           ("f16", "e4m3", False), ("f16", "e4m3", True)])
+def test_bad_block_id_is_flagged_on_the_tensor_core_paths(qdt, kvdt, prefix):
+    """Table entries past the pool or negative, in split units of the tensor-core decode
+    and of the prefix-aware launch: the producer flags them and loads block 0 instead."""
+    w = _tiny(9, [40, 700, 1300, 1300], q_dtype=qdt, kv_dtype=kvdt)
+    st = gpu_state(w, prefix=prefix)
+    binding.pkv_get_device_status()          # clear
+    bad = st.block_tables.clone()
+    bad[1, 3] = w.num_blocks + 1000
+    bad[2, 0] = -5
+    st.block_tables.copy_(bad)
+    st.decode()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_BLOCK_ID
+    assert np.isfinite(st.out_f64()[0]).all()
+
+
 def test_context_above_max_context_len_is_clamped_and_flagged():
     w = _tiny(8, [40, 100])
     st = gpu_state(w)

@@ -202,6 +202,26 @@ def test_sequence_with_more_queries_than_context_is_flagged_and_skipped():
     assert np.abs(st.out_f64()[10:] - ref[10:]).max() <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("tree", [False, True])
+def test_bad_block_id_is_flagged_not_faulted(tree):
+    """A table entry past the pool: the TMA producer flags it and loads block 0 instead."""
+    rng = np.random.default_rng(32)
+    make = inputs.make_tree_verify if tree else inputs.make_multi_query
+    w = make("bad", rng, [300, 40], [20, 64], num_q_heads=8, num_kv_heads=2, head_dim=128,
+             block_size=16, dtype="bf16")
+    st = MultiQueryState(w)
+    st.run_setup()
+    st.append_step()
+    binding.pkv_get_device_status()          # clear
+    bad = st.block_tables.clone()
+    bad[0, 2] = w.num_blocks + 77
+    st.block_tables.copy_(bad)
+    st.attend()
+    torch.cuda.synchronize()
+    assert binding.pkv_get_device_status() & binding.DEV_BAD_BLOCK_ID
+    assert np.isfinite(st.out_f64()[w.query_start[1]:]).all()   # the other sequence
+
+
 def test_unsupported_shapes_and_types_are_refused():
     rng = np.random.default_rng(27)
     w = inputs.make_multi_query("f32", rng, [5], [3], num_q_heads=2, num_kv_heads=2,
