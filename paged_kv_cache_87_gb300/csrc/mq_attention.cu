@@ -68,7 +68,7 @@ constexpr int kOffRing = kOffQ + 2 * kTileBytes;
 constexpr int kOffBars = kOffRing + kStages * kTileBytes;
 constexpr int kOffItems = kOffBars + 256;             // the two-slot ring of decoded items
 constexpr int kSmem = kOffItems + 2 * 64 + 1024;      // barriers, TMEM slot, flag; item ring; alignment
-constexpr int kThreads = 384;                         // 8 row warps; producer, MMA, 2 idle
+constexpr int kThreads = 384;                         // 8 row warps; producer, MMA, Q prefetch, idle
 // registers per thread after the split: the row warpgroups take what the third
 // warpgroup gives back (216 x 256 + 72 x 128 = 168 x 384, the launch's budget)
 constexpr int kRowRegs = 216;
