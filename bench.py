@@ -277,9 +277,10 @@ def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int =
                     caches=None):
     """Time the fp64 oracle on whole (sequence, kv head) units of the workload.
 
-    Returns (GB/s of KV read, seconds, bytes, threads, description).  The
-    sample's pool is built (untimed) by the oracle's own reshape_and_cache /
-    copy_blocks, or taken from `caches`.
+    Returns (GB/s of KV read, seconds, bytes, threads, description, single-thread
+    GB/s).  The single-thread figure is the calibration run: one (sequence, kv head)
+    unit on one thread.  The sample's pool is built (untimed) by the oracle's own
+    reshape_and_cache / copy_blocks, or taken from `caches`.
     """
     from tests.helpers import oracle_caches, oracle_decode
     nthreads = nthreads or os.cpu_count() or 1
@@ -293,7 +294,9 @@ def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int =
     sel0 = np.array([[s0, h] for h in range(G)], np.int32)
     t = time.perf_counter()
     oracle_decode(w, kc, vc, sel=sel0, nthreads=1)
-    per_token_s = (time.perf_counter() - t) / max(1, int(w.context_lens[s0]))
+    secs0 = time.perf_counter() - t
+    per_token_s = secs0 / max(1, int(w.context_lens[s0]))
+    single_gbs = int(w.context_lens[s0]) * w.head_dim * e * 2 / max(secs0, 1e-9) / 1e9
     budget_tokens = target_s * nthreads / max(per_token_s, 1e-9)
     units, tokens = [], 0
     for s in order:
@@ -311,7 +314,7 @@ def oracle_baseline(w, target_s: float, nthreads: int | None = None, seed: int =
     nbytes = sum(int(w.context_lens[s]) for s, _ in units) * w.head_dim * e * 2
     desc = (f"{len(units)} (sequence, kv head) units of the workload, {tokens} context tokens, "
             f"{len(sel)} query heads, fp64 oracle on {nthreads} threads")
-    return nbytes / secs / 1e9, secs, nbytes, nthreads, desc
+    return nbytes / secs / 1e9, secs, nbytes, nthreads, desc, single_gbs
 
 
 # ------------------------------------------------------------------- arms --
@@ -542,10 +545,12 @@ def run_ours(args, rank, world, local):
     if per_config:
         line["per_config"] = per_config
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, secs, nbytes, threads, desc = oracle_baseline(w, args.cpu_seconds)
+        v, secs, nbytes, threads, desc, single = oracle_baseline(w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc,
-                                "seconds": round(secs, 2)}
+                                "seconds": round(secs, 2),
+                                "single_thread": {"value": round(single, 4), "unit": "GB/s",
+                                                  "sample": "one (sequence, kv head) unit"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -782,7 +787,7 @@ def run_reference(args, rank, world, local):
     per_step = max(0.2, min(4.0, 150.0 / max(1, args.steps + args.warmup)))
     vals, secs, desc, threads = [], [], "", 1
     for i in range(args.warmup + args.steps):
-        v, s, _, threads, desc = oracle_baseline(w, per_step, seed=i, caches=caches)
+        v, s, _, threads, desc, _ = oracle_baseline(w, per_step, seed=i, caches=caches)
         if i >= args.warmup:
             vals.append(v)
             secs.append(s)
